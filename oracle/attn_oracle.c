@@ -1,0 +1,245 @@
+/*
+ * attn_oracle.c -- plain, slow, fp64 CPU oracle for scaled-dot-product
+ * attention as the kernels of this library compute it.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library links or calls this file;
+ * only the tests, the package smoke check and the benchmark's CPU-baseline
+ * leg do.  It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it computes, per (sequence or prompt b, query head h, query i), with
+ * every input value widened exactly to double:
+ *
+ *   g      = h / (Hq / Hkv)                          GQA: contiguous head groups
+ *   keep(j)= j < L  and (causal -> j <= pos_i)
+ *                   and (window > 0 -> pos_i - j < window        if causal
+ *                                      |pos_i - j| < window      otherwise)
+ *   s_j    = scale * sum_d q[i,h,d] * k[j,g,d]
+ *   s_j    = c * tanh(s_j / c)                       only when softcap c > 0
+ *   m      = max_{keep} s_j
+ *   p_j    = exp(s_j - m)                            (0 where !keep)
+ *   o[i,h] = sum_j p_j v[j,g,:] / sum_j p_j,   lse = m + log(sum_j p_j)
+ *
+ * Sources (pages on the subject):
+ *   - doppler src/gpu/kernels/attention.js, createAttentionUniformBuffer:
+ *     the parameter block (numHeads, numKVHeads, headDim, kvLen, seqLen, scale,
+ *     causal, startPos, attnSoftcap with 0 = disabled, slidingWindow with
+ *     0 = disabled, kvStart, pageSize, kvLayout contiguous/ring/paged).
+ *   - doppler src/inference/pipelines/text/attention/run.js,
+ *     runLayerAttentionGPU: decode appends the new token's K/V before
+ *     attention, so the query position is kvLen-1; the sliding-window clamp
+ *     kvLen = min(kvLen, W), kvStart = total - kvLen keeps the W most recent
+ *     keys including the query's own; scale = 1/sqrt(query_pre_attn_scalar)
+ *     or 1/sqrt(headDim).
+ *   - doppler attention.js, executeAttentionTieredQuant: an int8 K/V tier with
+ *     separate K and V scale buffers (granularity: one f16 scale per
+ *     (token, kv-head); value = code * scale).
+ *   - rullama src/backend/dispatch/attention.rs, vision_attention_chained:
+ *     vision attention is the same computation without the causal mask.
+ *
+ * Decode caches:
+ *   contiguous: k[b][t][g][d],      scales [b][g][t]   (t < cap)
+ *   paged:      k[page][r][g][d],   scales [page][g][r]
+ *               page = page_table[b][t / P], r = t % P
+ *   (attention.js passes the page table and pageSize to the paged decode
+ *    variant; logical token t lives in row t % P of page table[t / P].)
+ *
+ * Parity pins: the tests check this file against closed forms, a brute-force
+ * library softmax on the full score matrix, mask enumeration, and layout
+ * equivalences; none of them calls back into this code to produce an
+ * expected value.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* IEEE-754 binary16 -> double, from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_f16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);                 /* subnormal: f * 2^-14 * 2^-10 */
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(f + 1024), e - 25);     /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* keep(j) for a query at position pos over keys 0..L-1 */
+static int oracle_keep(long pos, long j, long L, int causal, int window)
+{
+    if (j < 0 || j >= L) return 0;
+    if (causal && j > pos) return 0;
+    if (window > 0) {
+        long dist = pos - j;
+        if (!causal && dist < 0) dist = -dist;
+        if (dist >= window) return 0;
+    }
+    return 1;
+}
+
+/* Attention of one query row against L key/value rows (all double).
+ * Two passes: the max of the kept logits, then the weighted sums. */
+static void oracle_attend(const double* q, const double* K, const double* V,
+                          long L, int D, long pos, int causal, int window,
+                          double softcap, double scale, double* o, double* lse)
+{
+    double* s = (double*)malloc(sizeof(double) * (L > 0 ? L : 1));
+    double m = -INFINITY;
+    for (long j = 0; j < L; ++j) {
+        if (!oracle_keep(pos, j, L, causal, window)) { s[j] = -INFINITY; continue; }
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += q[d] * K[j * D + d];
+        double x = scale * dot;
+        if (softcap > 0.0) x = softcap * tanh(x / softcap);
+        s[j] = x;
+        if (x > m) m = x;
+    }
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (m == -INFINITY) {             /* nothing kept: zero output, lse = -inf */
+        *lse = -INFINITY;
+        free(s);
+        return;
+    }
+    double l = 0.0;
+    for (long j = 0; j < L; ++j) {
+        if (s[j] == -INFINITY) continue;
+        double p = exp(s[j] - m);
+        l += p;
+        for (int d = 0; d < D; ++d) o[d] += p * V[j * D + d];
+    }
+    for (int d = 0; d < D; ++d) o[d] /= l;
+    *lse = m + log(l);
+    free(s);
+}
+
+/* One cache element (token t of sequence b, kv head g, dim d) as double. */
+static double oracle_cache_value(const void* cache, const uint16_t* scales, int is_int8,
+                                 const int32_t* page_table, int P, int max_pages, long cap,
+                                 long n_pages, int b, long t, int g, int d, int Hkv, int D)
+{
+    long row_base, scale_idx;
+    if (page_table) {
+        long page = page_table[(long)b * max_pages + t / P];
+        long r = t % P;
+        if (page < 0 || page >= n_pages) return NAN;     /* invalid page id */
+        row_base = ((page * P + r) * Hkv + g) * (long)D;
+        scale_idx = (page * Hkv + g) * (long)P + r;
+    } else {
+        row_base = (((long)b * cap + t) * Hkv + g) * (long)D;
+        scale_idx = ((long)b * Hkv + g) * cap + t;
+    }
+    if (is_int8) {
+        double code = (double)((const int8_t*)cache)[row_base + d];
+        return code * oracle_f16_to_double(scales[scale_idx]);
+    }
+    return oracle_f16_to_double(((const uint16_t*)cache)[row_base + d]);
+}
+
+/*
+ * Decode: one new query per sequence, at position kv_len[b]-1.
+ * rows: n_rows (b, h) pairs to evaluate (rows_b/rows_h), or n_rows < 0 for all
+ * B*Hq in (b, h) row-major order.  out: [n][D], lse: [n].
+ * Returns 0, or -1 on an invalid argument.
+ */
+int oracle_decode(const uint16_t* q, const void* k, const void* v, int kv_int8,
+                  const uint16_t* k_scales, const uint16_t* v_scales,
+                  const int32_t* kv_len, const int32_t* page_table,
+                  int page_size, int max_pages, long cap, long n_pages,
+                  int B, int Hq, int Hkv, int D, int window, double softcap, double scale,
+                  int n_rows, const int32_t* rows_b, const int32_t* rows_h,
+                  double* out, double* lse, int n_threads)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return -1;
+    if (page_table && page_size <= 0) return -1;
+    int G = Hq / Hkv;
+    long n = n_rows < 0 ? (long)B * Hq : n_rows;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (long r = 0; r < n; ++r) {
+        int b = n_rows < 0 ? (int)(r / Hq) : rows_b[r];
+        int h = n_rows < 0 ? (int)(r % Hq) : rows_h[r];
+        int g = h / G;
+        long L = kv_len[b];
+        long cap_b = page_table ? (long)max_pages * page_size : cap;
+        if (L > cap_b) L = cap_b;
+        if (L < 0) L = 0;
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);
+        for (int d = 0; d < D; ++d)
+            qd[d] = oracle_f16_to_double(q[((long)b * Hq + h) * D + d]);
+        for (long t = 0; t < L; ++t)
+            for (int d = 0; d < D; ++d) {
+                Kd[t * D + d] = oracle_cache_value(k, k_scales, kv_int8, page_table, page_size,
+                                                   max_pages, cap, n_pages, b, t, g, d, Hkv, D);
+                Vd[t * D + d] = oracle_cache_value(v, v_scales, kv_int8, page_table, page_size,
+                                                   max_pages, cap, n_pages, b, t, g, d, Hkv, D);
+            }
+        /* decode is causal at position L-1: causal masks nothing inside L */
+        oracle_attend(qd, Kd, Vd, L, D, L - 1, 1, window, softcap, scale,
+                      out + r * D, lse + r);
+        free(qd); free(Kd); free(Vd);
+    }
+    return 0;
+}
+
+/*
+ * Prefill / vision: S queries at positions 0..S-1 over the same S keys.
+ * q [S][Hq][D], k/v [S][Hkv][D] (f16 bits).  rows: n_rows (i, h) pairs, or
+ * n_rows < 0 for all S*Hq in (i, h) row-major order.  out: [n][D], lse: [n].
+ */
+int oracle_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   int S, int Hq, int Hkv, int D, int causal, int window,
+                   double softcap, double scale,
+                   int n_rows, const int32_t* rows_i, const int32_t* rows_h,
+                   double* out, double* lse, int n_threads)
+{
+    if (S < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return -1;
+    int G = Hq / Hkv;
+    long n = n_rows < 0 ? (long)S * Hq : n_rows;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 4)
+#endif
+    for (long r = 0; r < n; ++r) {
+        int i = n_rows < 0 ? (int)(r / Hq) : rows_i[r];
+        int h = n_rows < 0 ? (int)(r % Hq) : rows_h[r];
+        int g = h / G;
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1) * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1) * D);
+        for (int d = 0; d < D; ++d)
+            qd[d] = oracle_f16_to_double(q[((long)i * Hq + h) * D + d]);
+        for (long j = 0; j < S; ++j)
+            for (int d = 0; d < D; ++d) {
+                Kd[j * D + d] = oracle_f16_to_double(k[(j * Hkv + g) * (long)D + d]);
+                Vd[j * D + d] = oracle_f16_to_double(v[(j * Hkv + g) * (long)D + d]);
+            }
+        oracle_attend(qd, Kd, Vd, S, D, i, causal, window, softcap, scale,
+                      out + r * D, lse + r);
+        free(qd); free(Kd); free(Vd);
+    }
+    return 0;
+}
+
+/* Number of threads OpenMP would use (for reporting the CPU baseline). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

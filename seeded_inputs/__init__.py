@@ -1,0 +1,310 @@
+"""Seeded synthetic inputs for the attention kernels and for the oracle.
+
+This module is shared by the CUDA path's tests/benchmark and by the oracle's
+tests.  It holds no attention arithmetic: it only draws random numbers, encodes
+K/V into the int8 storage format the library consumes, and lays tensors out in
+the contiguous or paged cache layouts.
+
+Value recipe (the same for every workload):
+
+* Q, K, V elements are N(0, 1) draws rounded to float16 (round-to-nearest-even),
+  drawn from a ``torch.Generator`` seeded with the workload's seed.  Small cases
+  are drawn on the CPU; full-size workloads may be drawn on the GPU (the oracle
+  then reads the same bytes back, so both sides always see identical inputs).
+* int8 K/V: each (token, kv-head) row of D f16 values x is encoded as
+  ``s = f16(max|x| / 127)``, ``q = clamp(rint(x / float(s)), -127, 127)``
+  (rint = round-half-even, division in fp32), ``q = 0`` where ``s == 0``.
+  The attention inputs are then the dequantised values ``q * float(s)``; both
+  the oracle and the kernels dequantise from (q, s) themselves.
+* Paged caches: page ids come from a seeded random permutation of the page pool;
+  sequence b takes the next ``ceil(L_b / P)`` ids in order; unused page-table
+  slots hold -1.
+* Variable lengths: ``kv_len[b]`` uniform on the integers of [lo, hi].
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "f16_normal",
+    "quantize_int8_rows",
+    "DecodeCase",
+    "PrefillCase",
+    "make_decode_case",
+    "make_prefill_case",
+    "paged_from_contiguous",
+    "WORKLOADS",
+]
+
+
+def _gen(seed: int, device: str) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def f16_normal(shape, seed: int, device: str = "cpu", chunk: int = 1 << 26) -> torch.Tensor:
+    """N(0,1) float16 tensor drawn from a seeded generator.
+
+    Drawn in float32 and rounded to float16 (RNE); large tensors are drawn in
+    chunks to bound the float32 temporary.
+    """
+    g = _gen(seed, device)
+    out = torch.empty(shape, dtype=torch.float16, device=device)
+    flat = out.view(-1)
+    n = flat.numel()
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        flat[s:e] = torch.randn(e - s, generator=g, device=device, dtype=torch.float32).to(torch.float16)
+    return out
+
+
+def quantize_int8_rows(x: torch.Tensor, chunk_rows: int = 1 << 20):
+    """Encode f16 rows (last dim) as symmetric int8 with one f16 scale per row.
+
+    Returns (codes int8 same shape, scales f16 shape[:-1]).  See the module
+    docstring for the exact rule.
+    """
+    assert x.dtype == torch.float16
+    D = x.shape[-1]
+    rows = x.reshape(-1, D)
+    codes = torch.empty(rows.shape, dtype=torch.int8, device=x.device)
+    scales = torch.empty(rows.shape[0], dtype=torch.float16, device=x.device)
+    for s in range(0, rows.shape[0], chunk_rows):
+        e = min(rows.shape[0], s + chunk_rows)
+        xf = rows[s:e].float()
+        amax = xf.abs().amax(dim=1)
+        sc = (amax / 127.0).to(torch.float16)
+        scf = sc.float()
+        safe = torch.where(scf > 0, scf, torch.ones_like(scf))
+        qv = torch.round(xf / safe[:, None]).clamp_(-127, 127)
+        qv = torch.where(scf[:, None] > 0, qv, torch.zeros_like(qv))
+        codes[s:e] = qv.to(torch.int8)
+        scales[s:e] = sc
+    return codes.view(x.shape), scales.view(x.shape[:-1])
+
+
+@dataclass
+class DecodeCase:
+    """Inputs of one decode call (all tensors on one device).
+
+    Layouts (row-major):
+      q            f16 [B, Hq, D]
+      k, v         contiguous: [B, cap, Hkv, D]; paged: [n_pages, P, Hkv, D]
+                   (f16, or int8 codes when ``int8``)
+      k_scales/v_scales  f16; contiguous [B, Hkv, cap]; paged [n_pages, Hkv, P]
+      kv_len       int32 [B]
+      page_table   int32 [B, max_pages] or None
+    """
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    kv_len: torch.Tensor
+    batch: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    cap: int
+    int8: bool = False
+    k_scales: Optional[torch.Tensor] = None
+    v_scales: Optional[torch.Tensor] = None
+    page_table: Optional[torch.Tensor] = None
+    page_size: int = 0
+    max_pages: int = 0
+    window: int = 0
+    softcap: float = 0.0
+    scale: float = 0.0
+    lens: list = field(default_factory=list)
+
+    @property
+    def paged(self) -> bool:
+        return self.page_table is not None
+
+    @property
+    def n_pages(self) -> int:
+        return int(self.k.shape[0]) if self.paged else 0
+
+    def to(self, device: str) -> "DecodeCase":
+        kw = dict(self.__dict__)
+        for name in ("q", "k", "v", "kv_len", "k_scales", "v_scales", "page_table"):
+            t = kw[name]
+            if t is not None:
+                kw[name] = t.to(device)
+        return DecodeCase(**kw)
+
+
+@dataclass
+class PrefillCase:
+    """Inputs of one prefill / vision call: q f16 [S, Hq, D]; k, v f16 [S, Hkv, D]."""
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    seq_len: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    causal: bool
+    window: int = 0
+    softcap: float = 0.0
+    scale: float = 0.0
+
+    def to(self, device: str) -> "PrefillCase":
+        kw = dict(self.__dict__)
+        for name in ("q", "k", "v"):
+            kw[name] = kw[name].to(device)
+        return PrefillCase(**kw)
+
+
+def _lengths(batch: int, lo: int, hi: int, seed: int) -> list:
+    g = _gen(seed * 7919 + 17, "cpu")
+    return torch.randint(lo, hi + 1, (batch,), generator=g).tolist()
+
+
+def make_decode_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int,
+                     lens, seed: int, *, cap: Optional[int] = None, int8: bool = False,
+                     page_size: int = 0, n_pages: Optional[int] = None,
+                     window: int = 0, softcap: float = 0.0, scale: Optional[float] = None,
+                     device: str = "cpu") -> DecodeCase:
+    """Build a decode case.
+
+    ``lens`` is a list of per-sequence KV lengths, or a (lo, hi) tuple for
+    seeded uniform lengths.  With ``page_size > 0`` the cache is paged: a pool of
+    ``n_pages`` pages (default: just enough) filled with N(0,1) values, and a
+    seeded permutation assigning pages to sequences.
+    """
+    if isinstance(lens, tuple):
+        lens = _lengths(batch, lens[0], lens[1], seed)
+    lens = [int(x) for x in lens]
+    assert len(lens) == batch
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    q = f16_normal((batch, n_heads, head_dim), seed * 1000 + 1, device)
+    kv_len = torch.tensor(lens, dtype=torch.int32, device=device)
+    if page_size <= 0:
+        if cap is None:
+            cap = max(max(lens), 1)
+            cap = (cap + 7) // 8 * 8
+        k = f16_normal((batch, cap, n_kv_heads, head_dim), seed * 1000 + 2, device)
+        v = f16_normal((batch, cap, n_kv_heads, head_dim), seed * 1000 + 3, device)
+        ks = vs = None
+        if int8:
+            k, ks = quantize_int8_rows(k)
+            v, vs = quantize_int8_rows(v)
+            ks = ks.permute(0, 2, 1).contiguous()   # [B, Hkv, cap]
+            vs = vs.permute(0, 2, 1).contiguous()
+        return DecodeCase(q=q, k=k, v=v, kv_len=kv_len, batch=batch, n_heads=n_heads,
+                          n_kv_heads=n_kv_heads, head_dim=head_dim, cap=cap, int8=int8,
+                          k_scales=ks, v_scales=vs, window=window, softcap=softcap,
+                          scale=float(scale), lens=lens)
+    P = page_size
+    need = [(L + P - 1) // P for L in lens]
+    max_pages = max(max(need), 1)
+    if n_pages is None:
+        n_pages = max(sum(need), 1)
+    assert sum(need) <= n_pages
+    perm = torch.randperm(n_pages, generator=_gen(seed * 1000 + 4, "cpu"))
+    pt = torch.full((batch, max_pages), -1, dtype=torch.int32)
+    pos = 0
+    for b in range(batch):
+        pt[b, :need[b]] = perm[pos:pos + need[b]].to(torch.int32)
+        pos += need[b]
+    k = f16_normal((n_pages, P, n_kv_heads, head_dim), seed * 1000 + 2, device)
+    v = f16_normal((n_pages, P, n_kv_heads, head_dim), seed * 1000 + 3, device)
+    ks = vs = None
+    if int8:
+        k, ks = quantize_int8_rows(k)
+        v, vs = quantize_int8_rows(v)
+        ks = ks.permute(0, 2, 1).contiguous()        # [n_pages, Hkv, P]
+        vs = vs.permute(0, 2, 1).contiguous()
+    return DecodeCase(q=q, k=k, v=v, kv_len=kv_len, batch=batch, n_heads=n_heads,
+                      n_kv_heads=n_kv_heads, head_dim=head_dim, cap=max_pages * P, int8=int8,
+                      k_scales=ks, v_scales=vs, page_table=pt.to(device), page_size=P,
+                      max_pages=max_pages, window=window, softcap=softcap,
+                      scale=float(scale), lens=lens)
+
+
+def paged_from_contiguous(case: DecodeCase, page_size: int, seed: int,
+                          extra_pages: int = 3) -> DecodeCase:
+    """Scatter a contiguous case into a paged pool holding the same values.
+
+    Every logical token keeps its K/V (and scale) values, so attention over the
+    paged case must equal attention over the contiguous one exactly.
+    """
+    assert not case.paged
+    P = page_size
+    B, Hkv, D = case.batch, case.n_kv_heads, case.head_dim
+    max_pages = (case.cap + P - 1) // P
+    n_pages = B * max_pages + extra_pages
+    perm = torch.randperm(n_pages, generator=_gen(seed * 1000 + 5, "cpu"))
+    pt = perm[:B * max_pages].view(B, max_pages).to(torch.int32)
+    dev = case.k.device
+    pool_shape = (n_pages, P, Hkv, D)
+    kp = torch.zeros(pool_shape, dtype=case.k.dtype, device=dev)
+    vp = torch.zeros(pool_shape, dtype=case.v.dtype, device=dev)
+    ksp = vsp = None
+    if case.int8:
+        ksp = torch.zeros((n_pages, Hkv, P), dtype=torch.float16, device=dev)
+        vsp = torch.zeros((n_pages, Hkv, P), dtype=torch.float16, device=dev)
+    for b in range(B):
+        for i in range(max_pages):
+            t0, t1 = i * P, min((i + 1) * P, case.cap)
+            pg = int(pt[b, i])
+            kp[pg, :t1 - t0] = case.k[b, t0:t1]
+            vp[pg, :t1 - t0] = case.v[b, t0:t1]
+            if case.int8:
+                ksp[pg, :, :t1 - t0] = case.k_scales[b, :, t0:t1]
+                vsp[pg, :, :t1 - t0] = case.v_scales[b, :, t0:t1]
+    kw = dict(case.__dict__)
+    kw.update(k=kp, v=vp, k_scales=ksp, v_scales=vsp, page_table=pt.to(dev),
+              page_size=P, max_pages=max_pages, cap=max_pages * P)
+    return DecodeCase(**kw)
+
+
+def make_prefill_case(seq_len: int, n_heads: int, n_kv_heads: int, head_dim: int, seed: int, *,
+                      causal: bool, window: int = 0, softcap: float = 0.0,
+                      scale: Optional[float] = None, device: str = "cpu") -> PrefillCase:
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    q = f16_normal((seq_len, n_heads, head_dim), seed * 1000 + 11, device)
+    k = f16_normal((seq_len, n_kv_heads, head_dim), seed * 1000 + 12, device)
+    v = f16_normal((seq_len, n_kv_heads, head_dim), seed * 1000 + 13, device)
+    return PrefillCase(q=q, k=k, v=v, seq_len=seq_len, n_heads=n_heads, n_kv_heads=n_kv_heads,
+                       head_dim=head_dim, causal=causal, window=window, softcap=softcap,
+                       scale=float(scale))
+
+
+# The five seeded workloads, named by what they are.  Seeds are the workload
+# numbers 1..5.
+WORKLOADS = {
+    "tiny_decode": dict(kind="decode", seed=1, batch=1, n_heads=4, n_kv_heads=2, head_dim=64,
+                        lens=[128], int8=False, page_size=0, window=0, softcap=0.0,
+                        scale=1.0 / 8.0),
+    "vision_2304": dict(kind="prefill", seed=2, seq_len=2304, n_heads=16, n_kv_heads=16,
+                        head_dim=64, causal=False, window=0, softcap=0.0, scale=1.0 / 8.0),
+    "paged_gqa_decode": dict(kind="decode", seed=3, batch=32, n_heads=32, n_kv_heads=8,
+                             head_dim=128, lens=(512, 8192), int8=False, page_size=16,
+                             n_pages=32768, window=0, softcap=0.0,
+                             scale=1.0 / math.sqrt(128.0)),
+    "swa_softcap_prefill": dict(kind="prefill", seed=4, seq_len=4096, n_heads=8, n_kv_heads=4,
+                                head_dim=256, causal=True, window=1024, softcap=50.0,
+                                scale=1.0 / 16.0),
+    "int8_long_decode": dict(kind="decode", seed=5, batch=16, n_heads=32, n_kv_heads=8,
+                             head_dim=128, lens=[32768] * 16, int8=True, page_size=0,
+                             window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
+}
+
+
+def make_workload(name: str, device: str = "cpu"):
+    w = dict(WORKLOADS[name])
+    kind = w.pop("kind")
+    seed = w.pop("seed")
+    if kind == "decode":
+        b, hq, hkv, d, lens = (w.pop("batch"), w.pop("n_heads"), w.pop("n_kv_heads"),
+                               w.pop("head_dim"), w.pop("lens"))
+        return make_decode_case(b, hq, hkv, d, lens, seed, device=device, **w)
+    s, hq, hkv, d = w.pop("seq_len"), w.pop("n_heads"), w.pop("n_kv_heads"), w.pop("head_dim")
+    return make_prefill_case(s, hq, hkv, d, seed, device=device, **w)

@@ -1,0 +1,371 @@
+"""Pins for the fp64 oracle (CPU only).
+
+Each test checks the oracle against something other than itself: the pages'
+own parameter arithmetic (tests/golden), closed forms, special cases that
+reduce to a library routine, mask enumeration by interval reasoning, brute
+force with scipy's softmax on the full score matrix, and layout equivalences.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+import seeded_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([float(x) for x in line.split()])
+    return rows
+
+
+def _decode_case_from_arrays(q, k, v, lens, scale, window=0, softcap=0.0):
+    """Contiguous f16 decode case from float arrays (rounded to f16)."""
+    q = torch.tensor(np.asarray(q), dtype=torch.float16)
+    k = torch.tensor(np.asarray(k), dtype=torch.float16)
+    v = torch.tensor(np.asarray(v), dtype=torch.float16)
+    B, Hq, D = q.shape
+    return si.DecodeCase(q=q, k=k, v=v, kv_len=torch.tensor(lens, dtype=torch.int32),
+                         batch=B, n_heads=Hq, n_kv_heads=k.shape[2], head_dim=D,
+                         cap=k.shape[1], window=window, softcap=softcap, scale=scale,
+                         lens=list(lens))
+
+
+def _prefill_case_from_arrays(q, k, v, causal, scale, window=0, softcap=0.0):
+    q = torch.tensor(np.asarray(q), dtype=torch.float16)
+    k = torch.tensor(np.asarray(k), dtype=torch.float16)
+    v = torch.tensor(np.asarray(v), dtype=torch.float16)
+    S, Hq, D = q.shape
+    return si.PrefillCase(q=q, k=k, v=v, seq_len=S, n_heads=Hq, n_kv_heads=k.shape[1],
+                          head_dim=D, causal=causal, window=window, softcap=softcap,
+                          scale=scale)
+
+
+# ---------------------------------------------------------------- brute force
+def _kept_set(pos, L, causal, window):
+    """Kept key positions, built as an interval (not via the oracle's predicate)."""
+    if causal:
+        lo = 0 if window <= 0 else max(0, pos - window + 1)
+        hi = min(L - 1, pos)
+    else:
+        lo = 0 if window <= 0 else max(0, pos - window + 1)
+        hi = L - 1 if window <= 0 else min(L - 1, pos + window - 1)
+    return set(range(lo, hi + 1))
+
+
+def _brute(qrows, K, V, positions, L, causal, window, softcap, scale, dtype=np.float64):
+    """Full score matrix + scipy softmax; qrows [n, D], K/V [L, D]."""
+    qrows = qrows.astype(dtype)
+    K = K.astype(dtype)
+    V = V.astype(dtype)
+    S = (qrows @ K.T) * dtype(scale)
+    if softcap > 0:
+        S = dtype(softcap) * np.tanh(S / dtype(softcap))
+    mask = np.full(S.shape, False)
+    for r, pos in enumerate(positions):
+        for j in _kept_set(pos, L, causal, window):
+            mask[r, j] = True
+    Sm = np.where(mask, S, -np.inf).astype(np.float64)
+    P = scipy.special.softmax(Sm, axis=1)
+    O = P @ V.astype(np.float64)
+    lse = scipy.special.logsumexp(Sm, axis=1)
+    return O, lse, P
+
+
+# ---------------------------------------------------------------- pins
+def test_f16_decoder_matches_numpy_for_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_double(int(b)) for b in bits])
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+
+
+def test_powers_of_two_worked_example():
+    (o0, o1, lse_ref), = _golden_rows("powers_of_two_example.txt")
+    q = [[[1.0, 0.0]]]
+    k = [[[[0.0, 0.0]], [[1.0, 0.0]], [[2.0, 0.0]]]]
+    v = [[[[1.0, 0.0]], [[0.0, 1.0]], [[1.0, 1.0]]]]
+    case = _decode_case_from_arrays(q, k, v, [3], scale=math.log(2.0))
+    out, lse = oracle.decode(case)
+    assert out[0, 0] == pytest.approx(o0, abs=1e-15)
+    assert out[0, 1] == pytest.approx(o1, abs=1e-15)
+    assert lse[0] == pytest.approx(lse_ref, abs=1e-15)
+
+
+def test_scale_rule_golden():
+    # the library takes the scale as an argument; the pages' rule for it
+    for scalar, head_dim, want in _golden_rows("scale_from_query_pre_attn_scalar.txt"):
+        got = 1.0 / math.sqrt(scalar) if scalar else 1.0 / math.sqrt(head_dim)
+        assert got == want
+
+
+@pytest.mark.parametrize("D", [4, 64])
+def test_single_key_returns_its_value_row(D):
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((1, 2, D))
+    k = rng.standard_normal((1, 5, 1, D))
+    v = rng.standard_normal((1, 5, 1, D))
+    case = _decode_case_from_arrays(q, k, v, [1], scale=0.3)
+    out, lse = oracle.decode(case)
+    v0 = case.v[0, 0, 0].double().numpy()
+    assert np.array_equal(out[0], v0) and np.array_equal(out[1], v0)
+    # prefill row 0 under a causal mask also sees exactly one key
+    pc = _prefill_case_from_arrays(rng.standard_normal((3, 1, D)), rng.standard_normal((3, 1, D)),
+                                   rng.standard_normal((3, 1, D)), causal=True, scale=0.7)
+    o, _ = oracle.prefill(pc, rows=[(0, 0)])
+    assert np.array_equal(o[0], pc.v[0, 0].double().numpy())
+
+
+def test_constant_values_return_that_value():
+    rng = np.random.default_rng(1)
+    D, L = 16, 37
+    vbar = rng.standard_normal(D)
+    q = rng.standard_normal((2, 4, D))
+    k = rng.standard_normal((2, L, 2, D))
+    v = np.broadcast_to(vbar, (2, L, 2, D))
+    case = _decode_case_from_arrays(q, k, v, [L, 11], scale=0.25, softcap=3.0, window=7)
+    out, _ = oracle.decode(case)
+    vb = case.v[0, 0, 0].double().numpy()
+    assert np.allclose(out, vb[None, :], rtol=0, atol=1e-14)
+
+
+def test_zero_scale_gives_mean_of_visible_rows():
+    rng = np.random.default_rng(2)
+    S, D, W = 9, 8, 4
+    pc = _prefill_case_from_arrays(rng.standard_normal((S, 2, D)), rng.standard_normal((S, 1, D)),
+                                   rng.standard_normal((S, 1, D)), causal=True, scale=0.0,
+                                   window=W)
+    out, lse = oracle.prefill(pc)
+    V = pc.v[:, 0].double().numpy()
+    for i in range(S):
+        lo = max(0, i - W + 1)
+        want = V[lo:i + 1].mean(axis=0)
+        assert np.allclose(out[i * 2], want, atol=1e-15, rtol=0)
+        assert np.allclose(out[i * 2 + 1], want, atol=1e-15, rtol=0)
+        assert lse[i * 2] == pytest.approx(math.log(i + 1 - lo), abs=1e-15)
+
+
+def _one_hot_prefill(S, causal, window, softcap=0.0, seed=3):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((S, 1, S))
+    k = rng.standard_normal((S, 1, S))
+    v = np.eye(S)[:, None, :]            # v_j = e_j  => output row = weights
+    return _prefill_case_from_arrays(q, k, v, causal=causal, scale=0.2, window=window,
+                                     softcap=softcap)
+
+
+@pytest.mark.parametrize("causal,window", [(True, 0), (True, 1), (True, 3), (False, 0),
+                                           (False, 2), (False, 5)])
+def test_mask_enumeration_and_weights_sum_to_one(causal, window):
+    S = 12
+    pc = _one_hot_prefill(S, causal, window)
+    W, _ = oracle.prefill(pc)
+    for i in range(S):
+        kept = {j for j in range(S) if W[i, j] != 0.0}
+        assert kept == _kept_set(i, S, causal, window)
+        assert np.all(W[i] >= 0)
+        assert W[i].sum() == pytest.approx(1.0, abs=1e-14)
+
+
+def test_causal_window_pair_count():
+    # causal row i keeps i+1 keys; with a window, min(i+1, W)
+    S, Wn = 16, 5
+    pc = _one_hot_prefill(S, True, Wn)
+    W, _ = oracle.prefill(pc)
+    counts = (W != 0).sum(axis=1)
+    assert list(counts) == [min(i + 1, Wn) for i in range(S)]
+
+
+def test_decode_window_clamp_golden():
+    for total, window, kv_start, kept_len in _golden_rows("window_clamp.txt"):
+        total, window, kv_start, kept_len = int(total), int(window), int(kv_start), int(kept_len)
+        D = max(total, 2)
+        rng = np.random.default_rng(total * 100 + window)
+        q = rng.standard_normal((1, 1, D))
+        k = rng.standard_normal((1, total, 1, D))
+        v = np.eye(D)[:total][None, :, None, :]
+        case = _decode_case_from_arrays(q, k, v, [total], scale=0.1, window=window)
+        out, _ = oracle.decode(case)
+        kept = [j for j in range(total) if out[0, j] != 0.0]
+        assert kept == list(range(kv_start, kv_start + kept_len))
+
+
+def test_softcap_saturation_closed_form():
+    # c = 1 and logits of +-1000: tanh saturates to +-1 in double, so the two
+    # weights are 1 : e^2 regardless of the raw logits.
+    D = 2
+    q = [[[1.0, 0.0]]]
+    k = [[[[-1000.0, 0.0]], [[1000.0, 0.0]]]]
+    v = [[[[1.0, 0.0]], [[0.0, 1.0]]]]
+    case = _decode_case_from_arrays(q, k, v, [2], scale=1.0, softcap=1.0)
+    out, lse = oracle.decode(case)
+    e2 = math.exp(2.0)
+    assert out[0, 0] == pytest.approx(1.0 / (1.0 + e2), abs=1e-15)
+    assert out[0, 1] == pytest.approx(e2 / (1.0 + e2), abs=1e-15)
+    assert lse[0] == pytest.approx(1.0 + math.log(1.0 + math.exp(-2.0)), abs=1e-14)
+    # without the cap the large logit wins outright
+    nocap = _decode_case_from_arrays(q, k, v, [2], scale=1.0, softcap=0.0)
+    o2, _ = oracle.decode(nocap)
+    assert o2[0, 0] == 0.0 and o2[0, 1] == 1.0
+
+
+def test_huge_softcap_equals_no_cap():
+    case = si.make_decode_case(2, 4, 2, 16, [9, 30], seed=7)
+    a, la = oracle.decode(case)
+    case.softcap = 1e12
+    b, lb = oracle.decode(case)
+    assert np.allclose(a, b, atol=1e-12, rtol=0) and np.allclose(la, lb, atol=1e-12)
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,D,causal,window,softcap", [
+    (1, 1, 1, 4, True, 0, 0.0),
+    (5, 4, 2, 8, True, 0, 0.0),
+    (17, 6, 3, 16, True, 3, 2.5),
+    (17, 4, 1, 16, False, 0, 0.0),
+    (13, 2, 2, 8, False, 4, 1.5),
+    (33, 8, 2, 32, True, 8, 0.0),
+])
+def test_prefill_matches_brute_force(S, Hq, Hkv, D, causal, window, softcap):
+    pc = si.make_prefill_case(S, Hq, Hkv, D, seed=S * 10 + Hq, causal=causal, window=window,
+                              softcap=softcap, scale=0.37)
+    out, lse = oracle.prefill(pc)
+    q = pc.q.double().numpy()
+    K = np.repeat(pc.k.double().numpy(), Hq // Hkv, axis=1)    # explicit repeat-KV
+    V = np.repeat(pc.v.double().numpy(), Hq // Hkv, axis=1)
+    for h in range(Hq):
+        for dt in (np.float64, np.longdouble):
+            O, L, _ = _brute(q[:, h], K[:, h], V[:, h], list(range(S)), S, causal, window,
+                             softcap, 0.37, dtype=dt)
+            assert np.allclose(out[h::Hq], O, atol=1e-12, rtol=0)
+            assert np.allclose(lse[h::Hq], L, atol=1e-12, rtol=0)
+
+
+def _dequant_contiguous(case):
+    """Float64 K/V [B, cap, Hkv, D] from a contiguous case (int8: codes * scales)."""
+    if case.int8:
+        ks = case.k_scales.double().numpy().transpose(0, 2, 1)[..., None]   # [B, cap, Hkv, 1]
+        vs = case.v_scales.double().numpy().transpose(0, 2, 1)[..., None]
+        return case.k.numpy().astype(np.float64) * ks, case.v.numpy().astype(np.float64) * vs
+    return case.k.double().numpy(), case.v.double().numpy()
+
+
+@pytest.mark.parametrize("int8", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,D,lens,window,softcap", [
+    (1, 4, 2, 64, [128], 0, 0.0),
+    (3, 8, 2, 16, [1, 17, 40], 0, 0.0),
+    (2, 6, 3, 8, [25, 9], 6, 0.0),
+    (2, 4, 4, 32, [50, 33], 0, 4.0),
+])
+def test_decode_matches_brute_force(int8, B, Hq, Hkv, D, lens, window, softcap):
+    case = si.make_decode_case(B, Hq, Hkv, D, lens, seed=B * 31 + D, int8=int8,
+                               window=window, softcap=softcap, scale=0.21)
+    out, lse = oracle.decode(case)
+    K, V = _dequant_contiguous(case)
+    q = case.q.double().numpy()
+    G = Hq // Hkv
+    for b in range(B):
+        L = lens[b]
+        for h in range(Hq):
+            O, LS, _ = _brute(q[b, h][None], K[b, :L, h // G], V[b, :L, h // G], [L - 1], L,
+                              True, window, softcap, 0.21)
+            assert np.allclose(out[b * Hq + h], O[0], atol=1e-12, rtol=0)
+            assert lse[b * Hq + h] == pytest.approx(LS[0], abs=1e-12)
+
+
+@pytest.mark.parametrize("int8", [False, True])
+@pytest.mark.parametrize("page_size", [1, 8, 16])
+def test_paged_layout_equals_contiguous_exactly(int8, page_size):
+    case = si.make_decode_case(3, 4, 2, 16, [5, 33, 20], seed=11, int8=int8, cap=40)
+    paged = si.paged_from_contiguous(case, page_size, seed=12)
+    a, la = oracle.decode(case)
+    b, lb = oracle.decode(paged)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+def test_seeded_paged_case_matches_brute_force():
+    case = si.make_decode_case(4, 4, 2, 16, (3, 60), seed=13, page_size=8, int8=True)
+    out, _ = oracle.decode(case)
+    pt = case.page_table.numpy()
+    kc, vc = case.k.numpy().astype(np.float64), case.v.numpy().astype(np.float64)
+    ks, vs = case.k_scales.double().numpy(), case.v_scales.double().numpy()
+    q = case.q.double().numpy()
+    for b, L in enumerate(case.lens):
+        rows = [(pt[b, t // 8], t % 8) for t in range(L)]
+        for h in range(4):
+            g = h // 2
+            K = np.stack([kc[p, r, g] * ks[p, g, r] for p, r in rows])
+            V = np.stack([vc[p, r, g] * vs[p, g, r] for p, r in rows])
+            O, _, _ = _brute(q[b, h][None], K, V, [L - 1], L, True, 0, 0.0, case.scale)
+            assert np.allclose(out[b * 4 + h], O[0], atol=1e-12, rtol=0)
+
+
+def test_gqa_mapping_contiguous_groups():
+    # permuting kv heads, with the query-head groups permuted alongside,
+    # permutes the outputs the same way (mapping g = h // G)
+    case = si.make_decode_case(2, 6, 3, 8, [7, 12], seed=17)
+    out, _ = oracle.decode(case)
+    perm = [2, 0, 1]
+    G = 2
+    qperm = [perm[h // G] * G + h % G for h in range(6)]
+    pcase = si.make_decode_case(2, 6, 3, 8, [7, 12], seed=17)
+    pcase.k = case.k[:, :, perm].contiguous()
+    pcase.v = case.v[:, :, perm].contiguous()
+    pcase.q = case.q[:, qperm].contiguous()
+    pout, _ = oracle.decode(pcase)
+    out = out.reshape(2, 6, 8)
+    pout = pout.reshape(2, 6, 8)
+    assert np.array_equal(pout, out[:, qperm])
+    # G = 1 is plain multi-head attention: head h reads kv head h
+    mha = si.make_decode_case(1, 3, 3, 8, [9], seed=18)
+    o, _ = oracle.decode(mha)
+    K, V = mha.k.double().numpy(), mha.v.double().numpy()
+    for h in range(3):
+        O, _, _ = _brute(mha.q[0, h].double().numpy()[None], K[0, :9, h], V[0, :9, h], [8], 9,
+                         True, 0, 0.0, mha.scale)
+        assert np.allclose(o[h], O[0], atol=1e-12)
+
+
+def test_zero_length_sequence_gives_zeros():
+    case = si.make_decode_case(2, 2, 1, 8, [0, 4], seed=19, cap=8)
+    out, lse = oracle.decode(case)
+    assert np.all(out[:2] == 0) and np.all(np.isneginf(lse[:2]))
+    assert np.all(np.isfinite(out[2:]))
+
+
+def test_row_selection_matches_full_run():
+    pc = si.make_prefill_case(20, 4, 2, 16, seed=21, causal=True, window=6, softcap=5.0)
+    full, fl = oracle.prefill(pc)
+    rows = [(0, 0), (19, 3), (7, 2), (13, 1)]
+    part, pl = oracle.prefill(pc, rows=rows)
+    for n, (i, h) in enumerate(rows):
+        assert np.array_equal(part[n], full[i * 4 + h]) and pl[n] == fl[i * 4 + h]
+    case = si.make_decode_case(3, 4, 2, 16, [5, 9, 2], seed=22)
+    full, fl = oracle.decode(case)
+    part, pl = oracle.decode(case, rows=[(2, 3), (0, 1)])
+    assert np.array_equal(part[0], full[2 * 4 + 3]) and np.array_equal(part[1], full[1])
+
+
+def test_int8_encoding_rule():
+    # the generator's encoding: s = f16(max|x|/127), codes in [-127, 127],
+    # |x - code*s| <= s/2 (plus the f16 rounding of s), zero rows -> zero codes
+    x = si.f16_normal((64, 32), seed=23)
+    x[5] = 0
+    codes, scales = si.quantize_int8_rows(x)
+    xf, sf, cf = x.double(), scales.double(), codes.double()
+    assert codes.abs().max() <= 127
+    assert torch.all(cf[5] == 0) and sf[5] == 0
+    err = (xf - cf * sf[:, None]).abs().max(dim=1).values
+    assert torch.all(err <= sf * 0.5 * (1 + 1e-3) + 1e-12)
