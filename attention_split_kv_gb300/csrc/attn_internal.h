@@ -1,0 +1,93 @@
+// attn_internal.h -- declarations shared by the libattn translation units
+// (host side only: launch descriptors, tensor-map encoding, error reporting).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "attn.h"
+
+namespace attn {
+
+// Error codes written to the device error word.
+enum : int {
+    kErrNone = 0,
+    kErrTimeoutLoad = 1,     // a consumer waited too long for a TMA tile
+    kErrTimeoutSlot = 2,     // the producer waited too long for a free slot
+    kErrTimeoutMma = 3,      // a wait on a tensor-core result timed out
+    kErrTimeoutSoftmax = 4,  // the MMA issuer waited too long for P
+    kErrBadPage = 5,         // a page-table entry in use was outside the page pool
+};
+
+// Records a message for attn_last_error() (thread-local) and returns `st`.
+attn_status set_error(attn_status st, const char* fmt, ...);
+
+// Device error word (a file-scope __device__ int), as a device pointer.
+int* device_error_word();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// ---- tensor maps (cuTensorMapEncodeTiled through the runtime's driver entry point)
+// 3-D f16 map over a row-major [S, H, D] tensor: dims (D, H, S), box
+// (64, 1, box_rows), 128-byte swizzle (tensor-core operand layout).
+attn_status encode_tmap_3d_f16_sw128(CUtensorMap* map, const void* base, int D, int H, int S,
+                                     int box_rows);
+// Generic map, no swizzle, zero fill.  dims/strides in elements/bytes,
+// innermost first; strides[i] is the byte stride of dimension i+1.
+attn_status encode_tmap_plain(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int rank,
+                              const uint64_t* dims, const uint64_t* strides_bytes,
+                              const uint32_t* box);
+
+// ---- prefill
+struct PrefillLaunch {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    float* lse;
+    int S, Hq, Hkv, D, causal, window;
+    float softcap, scale;
+    int* err_word;
+    cudaStream_t stream;
+};
+attn_status launch_prefill(const PrefillLaunch& L);
+
+// ---- decode
+struct DecodeLaunch {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* k_scales;
+    const void* v_scales;
+    const int32_t* kv_len;
+    const int32_t* page_table;
+    int page_size, max_pages, n_pages, max_kv;
+    int int8;
+    int B, Hq, Hkv, D, window;
+    float softcap, scale;
+    int split_keys;
+    void* out;
+    float* lse;
+    void* workspace;
+    size_t workspace_bytes;
+    int* err_word;
+    cudaStream_t stream;
+};
+
+// Split plan shared by attn_decode_workspace_size and attn_decode.
+struct DecodePlan {
+    int GH;            // query heads handled together per kv head (1, 2 or 4)
+    int HG;            // head groups per kv head: G / GH
+    int split;         // keys per split (multiple of the 16-key tile)
+    long max_items;    // upper bound of work items
+    size_t off_lse, off_o, bytes;
+};
+bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys, DecodePlan* plan);
+attn_status launch_decode(const DecodeLaunch& L, const DecodePlan& plan);
+
+constexpr int kDecodeMaxBatch = 4096;
+
+}  // namespace attn

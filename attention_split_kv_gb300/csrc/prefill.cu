@@ -1,0 +1,431 @@
+// prefill.cu -- tiled causal / bidirectional attention (text prefill and the
+// vision tower) on the sm_103a tensor cores.
+//
+// Problem (doppler src/gpu/kernels/attention.js, the prefill tiers of
+// selectAttentionTier / executeAttention; rullama src/backend/dispatch/
+// attention.rs, vision_attention_chained and its flash variants): for every
+// query token i and head h, softmax over the kept keys j of
+// scale * q_i . k_j (optionally soft-capped), applied to v_j.  The pages'
+// kernels tile K/V through workgroup-shared memory and run an online softmax
+// with 1-16 queries per workgroup; here a CTA owns a 128-query tile and the
+// two contractions run on tcgen05:
+//
+//   S_j  = Q K_j^T     128 x BN, f32 in TMEM        (tcgen05.mma, A,B in smem)
+//   P_j  = exp2(S_j * scale*log2e - m)  f16 -> smem (4 softmax warps, 1 row/thread)
+//   O   += P_j V_j     128 x D,  f32 in TMEM        (tcgen05.mma, V MN-major)
+//
+// Roles (192 threads): warps 0-3 softmax + epilogue (thread t owns query row t
+// = TMEM lane t), warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer.
+// The MMA warp issues S_{j+1} before waiting for P_j, so QK^T of the next tile
+// overlaps the softmax of the current one.  O is rescaled lazily: only when a
+// row's running max grows by more than 8 (log2 units), so P <= 2^8 stays
+// exact in f16 range and the final O / l is unchanged.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;                 // queries per CTA (TMEM lanes)
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int D>
+struct PrefillCfg {
+    static constexpr int NCH = D / 64;                   // 64-element (128-byte) chunks of D
+    static constexpr int BN = (D == 256) ? 64 : 128;     // keys per tile
+    static constexpr int STAGES = (D == 64) ? 3 : 2;     // K/V ring depth
+    static constexpr int PCH = BN / 64;                  // 64-key chunks of a P row
+    static constexpr uint32_t Q_BYTES = NCH * BM * 128;
+    static constexpr uint32_t KV_CHUNK = BN * 128;       // one 64-column box of a K or V tile
+    static constexpr uint32_t KV_BYTES = NCH * KV_CHUNK; // one K (or V) tile
+    static constexpr uint32_t P_BYTES = PCH * BM * 128;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
+    static constexpr uint32_t OFF_P = OFF_V + STAGES * KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+    // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2], teardown
+    static constexpr int N_BARS = 1 + 3 * STAGES + 6 + 1;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
+    static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+    static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // slack for 1024-byte alignment
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_O = 2 * BN;
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(COL_O + D <= TMEM_COLS, "TMEM budget");
+    // one CTA per SM: two would not fit in the SM's shared memory, so a CTA
+    // never waits on another's 512 TMEM columns
+    static_assert(2 * SMEM_ALLOC > 233472, "one CTA per SM");
+};
+
+struct PrefillArgs {
+    __half* out;
+    float* lse;
+    int S, Hq, Hkv, causal, window;
+    float softcap, scale;
+    int scale_positive;
+    int* err;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
+    using C = PrefillCfg<D>;
+    constexpr int BN = C::BN, NCH = C::NCH, STAGES = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    const int B_QFULL = 0;
+    const int B_KFULL = 1, B_VFULL = 1 + STAGES, B_KVEMPTY = 1 + 2 * STAGES;
+    const int B_SFULL = 1 + 3 * STAGES, B_PFULL = B_SFULL + 2, B_PVDONE = B_SFULL + 4;
+    const int B_TEARDOWN = B_SFULL + 6;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = args.S;
+    const int n_qt = (S + BM - 1) / BM;
+    // causal tiles late in the sequence carry the most keys: launch them first
+    const int qt = args.causal ? (n_qt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    const int h = blockIdx.y;
+    const int g = h / (args.Hq / args.Hkv);
+    const int q0 = qt * BM;
+    const int q_last = min(q0 + BM - 1, S - 1);
+    const int W = args.window;
+    int hi = args.causal ? q_last + 1 : S;
+    if (!args.causal && W > 0) hi = min(S, q_last + W);
+    const int lo = W > 0 ? max(0, q0 - W + 1) : 0;
+    const int jt0 = lo / BN;
+    const int n_tiles = (hi + BN - 1) / BN - jt0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B_QFULL), 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar(B_KFULL + s), 1);
+            mbar_init(bar(B_VFULL + s), 1);
+            mbar_init(bar(B_KVEMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_SFULL + b), 1);
+            mbar_init(bar(B_PFULL + b), 4 * 32);
+            mbar_init(bar(B_PVDONE + b), 1);
+        }
+        mbar_init(bar(B_TEARDOWN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(bar(B_QFULL), C::Q_BYTES);
+            for (int c = 0; c < NCH; ++c)
+                tma_load_3d(sbase + C::OFF_Q + c * (BM * 128), &tm_q, bar(B_QFULL), c * 64, h, q0);
+            int issued = 0;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % STAGES;
+                if (j >= STAGES &&
+                    !mbar_wait(bar(B_KVEMPTY + st), ((j / STAGES) - 1) & 1, abort_flag, args.err, kErrTimeoutSlot))
+                    break;
+                const int key0 = (jt0 + j) * BN;
+                mbar_arrive_expect_tx(bar(B_KFULL + st), C::KV_BYTES);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(sbase + C::OFF_K + st * C::KV_BYTES + c * C::KV_CHUNK, &tm_k, bar(B_KFULL + st),
+                                c * 64, g, key0);
+                mbar_arrive_expect_tx(bar(B_VFULL + st), C::KV_BYTES);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(sbase + C::OFF_V + st * C::KV_BYTES + c * C::KV_CHUNK, &tm_v, bar(B_VFULL + st),
+                                c * 64, g, key0);
+                issued = j + 1;
+            }
+            if (*abort_flag) {
+                // let copies already in flight land before the CTA's shared memory goes away
+                mbar_wait(bar(B_QFULL), 0, abort_flag, args.err, kErrTimeoutLoad);
+                for (int j = max(0, issued - STAGES); j < issued; ++j) {
+                    const int st = j % STAGES;
+                    volatile int never = 0;
+                    mbar_wait(bar(B_KFULL + st), (j / STAGES) & 1, &never, args.err, kErrTimeoutLoad);
+                    mbar_wait(bar(B_VFULL + st), (j / STAGES) & 1, &never, args.err, kErrTimeoutLoad);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f16_f32(BM, BN, false);
+            constexpr uint32_t idesc_o = idesc_f16_f32(BM, D, true);
+            bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, args.err, kErrTimeoutLoad);
+            auto issue_s = [&](int j) {
+                const int st = j % STAGES;
+                const uint32_t d_tmem = tmem + (j & 1) * BN;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = smem_desc_sw128(sbase + C::OFF_Q + c * (BM * 128) + kk * 32, 16, 1024);
+                        const uint64_t b = smem_desc_sw128(
+                            sbase + C::OFF_K + st * C::KV_BYTES + c * C::KV_CHUNK + kk * 32, 16, 1024);
+                        tc_mma_f16_ss(d_tmem, a, b, idesc_s, (c | kk) != 0);
+                    }
+                }
+                tc_commit(bar(B_SFULL + (j & 1)));
+            };
+            if (ok && n_tiles > 0) {
+                ok = mbar_wait(bar(B_KFULL + 0), 0, abort_flag, args.err, kErrTimeoutLoad);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0);
+                }
+            }
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j + 1 < n_tiles) {
+                    const int st1 = (j + 1) % STAGES;
+                    if (!mbar_wait(bar(B_KFULL + st1), ((j + 1) / STAGES) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
+                    tc_fence_after();
+                    issue_s(j + 1);
+                }
+                if (!mbar_wait(bar(B_PFULL + (j & 1)), (j >> 1) & 1, abort_flag, args.err, kErrTimeoutSoftmax)) break;
+                const int st = j % STAGES;
+                if (!mbar_wait(bar(B_VFULL + st), (j / STAGES) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
+                tc_fence_after();
+                const uint32_t p_base = sbase + C::OFF_P + (j & 1) * C::P_BYTES;
+                const uint32_t v_base = sbase + C::OFF_V + st * C::KV_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t a = smem_desc_sw128(p_base + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
+                    tc_mma_f16_ss(tmem + C::COL_O, a, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(B_PVDONE + (j & 1)));
+                tc_commit(bar(B_KVEMPTY + st));
+            }
+            // all issued MMAs must retire before TMEM is released
+            tc_commit(bar(B_TEARDOWN));
+            volatile int never = 0;
+            mbar_wait(bar(B_TEARDOWN), 0, &never, args.err, kErrTimeoutMma);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const int row = threadIdx.x;           // 0..127 == TMEM lane
+        const int qi = q0 + row;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const bool capped = args.softcap > 0.f;
+        const float scale_log2 = args.scale * kLog2e;
+        const float cap_log2 = args.softcap * kLog2e;
+        const float inv_cap_scale = capped ? args.scale / args.softcap : 0.f;
+        float m_used = -INFINITY;   // running max actually used as the exponent offset (log2 units)
+        float l_sum = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            if (!mbar_wait(bar(B_SFULL + (j & 1)), (j >> 1) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
+            tc_fence_after();
+            float t[BN];
+            {
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    tc_ld_32x32b_x32(lane_base + (j & 1) * BN + c * 32, r);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) t[c * 32 + i] = __uint_as_float(r[i]);
+                }
+            }
+            const int key0 = (jt0 + j) * BN;
+            const int key_last = key0 + BN - 1;
+            bool full = key_last < S;
+            if (args.causal) full = full && key_last <= qi;
+            if (W > 0) full = full && (qi - key0 < W) && (args.causal || key_last - qi < W);
+            // scaled logits in log2 units
+            float mx = -INFINITY;
+            if (capped) {
+#pragma unroll
+                for (int i = 0; i < BN; ++i) t[i] = cap_log2 * tanh_abs_accurate(t[i] * inv_cap_scale);
+            } else if (!args.scale_positive) {
+#pragma unroll
+                for (int i = 0; i < BN; ++i) t[i] *= scale_log2;
+            }
+            if (!full) {
+#pragma unroll
+                for (int i = 0; i < BN; ++i) {
+                    const int kj = key0 + i;
+                    bool keep = kj < S;
+                    if (args.causal) keep = keep && kj <= qi;
+                    if (W > 0) {
+                        int dist = qi - kj;
+                        if (!args.causal && dist < 0) dist = -dist;
+                        keep = keep && dist < W;
+                    }
+                    if (!keep) t[i] = -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < BN; ++i) mx = fmaxf(mx, t[i]);
+            // raw-accumulator path: the max of raw logits scaled is the scaled max
+            const bool raw = !capped && args.scale_positive;
+            const float m_tile = raw ? mx * scale_log2 : mx;
+            const bool need = m_tile > m_used + kRescaleThreshold || (m_used == -INFINITY && m_tile > -INFINITY);
+            if (__any_sync(0xffffffffu, need)) {
+                const float m_new = need ? fmaxf(m_tile, m_used) : m_used;
+                const float alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
+                if (j > 0) {
+                    // O must not be in flight while it is rescaled
+                    if (!mbar_wait(bar(B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
+                    tc_fence_after();
+                    const float a = need ? alpha : 1.f;
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tc_ld_32x32b_x32(lane_base + C::COL_O + c * 32, r);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+                        tc_st_32x32b_x32(lane_base + C::COL_O + c * 32, r);
+                    }
+                    tc_wait_st();
+                }
+                if (need) {
+                    l_sum *= alpha;
+                    m_used = m_new;
+                }
+            }
+            const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
+            // P buffer (j & 1) is free once PV_{j-2} has retired
+            if (j >= 2 && !mbar_wait(bar(B_PVDONE + (j & 1)), ((j - 2) >> 1) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
+            uint8_t* prow = smem + C::OFF_P + (j & 1) * C::P_BYTES + row * 128;
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < C::PCH; ++c) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    uint32_t packed[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = c * 64 + u * 8 + e * 2;
+                        const float x0 = raw ? fmaf(t[i], scale_log2, -m_off) : t[i] - m_off;
+                        const float x1 = raw ? fmaf(t[i + 1], scale_log2, -m_off) : t[i + 1] - m_off;
+                        const __half2 hp = __floats2half2_rn(ex2_approx(x0), ex2_approx(x1));
+                        const float2 back = __half22float2(hp);
+                        lsum += back.x + back.y;
+                        packed[e] = *reinterpret_cast<const uint32_t*>(&hp);
+                    }
+                    const int sw = (u ^ (row & 7)) * 16;
+                    *reinterpret_cast<uint4*>(prow + c * (BM * 128) + sw) =
+                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                }
+            }
+            l_sum += lsum;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_PFULL + (j & 1)));
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok && n_tiles > 0) {
+            const int jl = n_tiles - 1;
+            ok = mbar_wait(bar(B_PVDONE + (jl & 1)), (jl >> 1) & 1, abort_flag, args.err, kErrTimeoutMma);
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+            __half* orow = args.out + (static_cast<size_t>(qi) * args.Hq + h) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tc_ld_32x32b_x32(lane_base + C::COL_O + c * 32, r);
+                tc_wait_ld();
+                if (qi < S) {
+                    uint32_t hv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const __half2 p2 = __floats2half2_rn(__uint_as_float(r[2 * i]) * inv_l,
+                                                             __uint_as_float(r[2 * i + 1]) * inv_l);
+                        hv[i] = *reinterpret_cast<const uint32_t*>(&p2);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+                }
+            }
+            if (args.lse && qi < S) {
+                args.lse[static_cast<size_t>(qi) * args.Hq + h] =
+                    l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+attn_status launch_prefill_d(const PrefillLaunch& L) {
+    using C = PrefillCfg<D>;
+    CUtensorMap tq, tk, tv;
+    attn_status st;
+    // 3-D maps over [S, H, D] f16: dims (D, H, S), 64-element x rows boxes, 128-byte swizzle
+    if ((st = encode_tmap_3d_f16_sw128(&tq, L.q, D, L.Hq, L.S, BM)) != ATTN_OK) return st;
+    if ((st = encode_tmap_3d_f16_sw128(&tk, L.k, D, L.Hkv, L.S, C::BN)) != ATTN_OK) return st;
+    if ((st = encode_tmap_3d_f16_sw128(&tv, L.v, D, L.Hkv, L.S, C::BN)) != ATTN_OK) return st;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM_ALLOC) != cudaSuccess)
+            return set_error(ATTN_ECUDA, "cudaFuncSetAttribute(prefill smem) failed");
+        attr_set[dev] = true;
+    }
+    PrefillArgs a;
+    a.out = static_cast<__half*>(L.out);
+    a.lse = L.lse;
+    a.S = L.S;
+    a.Hq = L.Hq;
+    a.Hkv = L.Hkv;
+    a.causal = L.causal;
+    a.window = L.window;
+    a.softcap = L.softcap;
+    a.scale = L.scale;
+    a.scale_positive = L.scale > 0.f;
+    a.err = L.err_word;
+    dim3 grid((L.S + BM - 1) / BM, L.Hq);
+    prefill_tc_kernel<D><<<grid, kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(ATTN_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status launch_prefill(const PrefillLaunch& L) {
+    switch (L.D) {
+        case 64: return launch_prefill_d<64>(L);
+        case 128: return launch_prefill_d<128>(L);
+        case 256: return launch_prefill_d<256>(L);
+        default: return set_error(ATTN_EUNSUPPORTED, "head_dim %d not supported (64, 128, 256)", L.D);
+    }
+}
+
+}  // namespace attn

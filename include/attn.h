@@ -1,0 +1,166 @@
+/*
+ * attn.h -- C ABI of libattn: scaled-dot-product attention for LLM decode,
+ * prefill and vision-tower inference on one NVIDIA GB300 (sm_103a).
+ *
+ * Every call is asynchronous on the caller's CUDA stream and allocates no
+ * device memory: the caller owns every buffer it passes.  Pointers named
+ * "device" must be device (or managed) addresses of the current CUDA device.
+ * "stream" is a cudaStream_t (CUstream) handle; NULL is the legacy default
+ * stream.  On a non-OK status nothing has been launched (argument errors are
+ * detected on the host before any launch) and attn_last_error() describes the
+ * problem.
+ *
+ * Notation: B batch, Hq query heads, Hkv kv heads (Hq % Hkv == 0, G = Hq/Hkv),
+ * D head_dim, L_b = kv_len[b], S prefill length, P page size, W window.
+ *
+ * What is computed (for each sequence/prompt b, query head h, query i):
+ *   g = h / G;  s_j = scale * (q_i . k_j[g]);  s_j = c*tanh(s_j/c) if c > 0;
+ *   o_i = sum_j softmax_j(s) v_j[g] over the kept keys j, in fp32 with f16 I/O.
+ * Sources: doppler src/gpu/kernels/attention.js (createAttentionUniformBuffer:
+ * numHeads, numKVHeads, headDim, kvLen, seqLen, scale, causal, attnSoftcap
+ * "0 = disabled", slidingWindow "0 = disabled", pageSize, kvLayout
+ * contiguous/paged; executeAttention: the per-call kvLen buffer and page
+ * table), doppler src/inference/pipelines/text/attention/run.js
+ * (runLayerAttentionGPU: the decode query sits at position kvLen-1, the
+ * sliding-window clamp, scale = 1/sqrt(query_pre_attn_scalar)), and rullama
+ * src/backend/dispatch/attention.rs (vision_attention_chained: bidirectional
+ * attention over [n_patches, n_heads, head_dim] tensors).
+ */
+#ifndef LIBATTN_ATTN_H
+#define LIBATTN_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_EINVAL = 1,        /* invalid argument (null pointer, bad size, bad count) */
+    ATTN_EUNSUPPORTED = 2,  /* valid but not supported (head_dim, page size, ...) */
+    ATTN_ECUDA = 3,         /* a CUDA runtime/driver call failed */
+    ATTN_EBOUNDS = 4,       /* device data out of range (attn_decode_validate) */
+    ATTN_ETIMEOUT = 5       /* a kernel abandoned a pipeline wait (attn_device_status) */
+} attn_status;
+
+typedef enum {
+    ATTN_KV_F16 = 0,        /* K/V cache elements are IEEE binary16 */
+    ATTN_KV_INT8 = 1        /* K/V cache elements are int8 codes with per-(token, kv-head)
+                               f16 scales: value = code * scale (attention.js,
+                               executeAttentionTieredQuant: int8 K/V with separate
+                               K and V scale buffers) */
+} attn_kv_dtype;
+
+/* Library version, e.g. "libattn 0.1.0 sm_103a". */
+const char* attn_version(void);
+
+/* Message for the last non-OK status returned on this host thread. */
+const char* attn_last_error(void);
+
+/*
+ * Bytes of scratch memory attn_decode needs for these sizes.  max_kv is the
+ * largest kv_len any sequence may have in the call; split_keys as in
+ * attn_decode (0 = automatic).  Returns 0 for invalid sizes.
+ */
+size_t attn_decode_workspace_size(int batch, int n_heads, int n_kv_heads, int head_dim,
+                                  int max_kv, int split_keys);
+
+/*
+ * attn_decode -- split-KV flash-decode: one new query token per sequence
+ * attends to that sequence's KV cache.
+ *
+ *  q           device, f16 [B, Hq, D] (row-major), the new tokens' queries.
+ *  k_cache,    device.  Contiguous layout (page_table == NULL):
+ *  v_cache       [B, max_kv, Hkv, D]; token t of sequence b at [b, t].
+ *                Paged layout: a pool [n_pages, P, Hkv, D]; token t of
+ *                sequence b at [page_table[b, t / P], t % P].
+ *                Elements f16 (ATTN_KV_F16) or int8 codes (ATTN_KV_INT8).
+ *  kv_len      device, int32 [B]: L_b, the number of cached tokens including
+ *                the new one (the query's position is L_b - 1, so the causal
+ *                mask keeps every cached token).  Values are clamped to the
+ *                layout's capacity; L_b <= 0 yields a zero output row and
+ *                lse = -inf.  attn_decode_validate checks them.
+ *  page_table  device, int32 [B, max_pages_per_seq], or NULL for contiguous.
+ *                Entries past ceil(L_b / P) are never read.
+ *  page_size   P: a power of two in [1, 1024] (>= 8 for int8 caches).
+ *  n_pages     pages in the pool (paged layout only).
+ *  max_kv      contiguous: tokens per sequence in the cache (capacity; a
+ *                multiple of 8 for int8 caches).  Paged: an upper bound on
+ *                L_b (<= max_pages_per_seq * P), used to size the split plan.
+ *  k_scales,   device f16, int8 caches only (else NULL).  Contiguous:
+ *  v_scales      [B, Hkv, max_kv]; paged: [n_pages, Hkv, P].
+ *  window      W > 0 keeps only the W most recent tokens (positions
+ *                L_b - W .. L_b - 1, run.js sliding-window clamp); 0 = off.
+ *  softcap     c > 0 applies s -> c * tanh(s / c) after scaling; 0 = off.
+ *  scale       the logit scale, e.g. 1/sqrt(D) or 1/sqrt(query_pre_attn_scalar).
+ *  split_keys  keys per split (a multiple of 16), or 0 for automatic.  The
+ *                result does not depend on it beyond fp32 rounding.
+ *  out         device, f16 [B, Hq, D].
+ *  lse_out     device, f32 [B, Hq] or NULL: log-sum-exp of the kept scaled
+ *                logits (natural log).
+ *  workspace   device scratch of workspace_bytes >= attn_decode_workspace_size(
+ *                B, Hq, Hkv, D, max_kv, split_keys); contents need no
+ *                initialisation and are overwritten.
+ *  D must be 64, 128 or 256; G = Hq / Hkv any positive integer.
+ *  The same split plan and arithmetic order are used for both layouts, so a
+ *  paged cache holding the same values as a contiguous one gives bit-identical
+ *  results.
+ */
+attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* kv_len, const int32_t* page_table,
+                        int page_size, int max_pages_per_seq, int n_pages, int max_kv,
+                        const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
+                        int batch, int n_heads, int n_kv_heads, int head_dim,
+                        int window, float softcap, float scale, int split_keys,
+                        void* out, float* lse_out,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_prefill -- tiled prefill / vision attention of S tokens over themselves
+ * on the tensor cores (tcgen05 + TMEM, operands staged by TMA).
+ *
+ *  q     device f16 [S, Hq, D];  k, v  device f16 [S, Hkv, D]  (token-major,
+ *        heads interleaved: the q/k/v layout vision_attention_chained shares
+ *        with text attention).
+ *  causal  nonzero: query i keeps keys j <= i (text prefill); 0: bidirectional
+ *          (vision tower).
+ *  window  W > 0: causal keeps i - W < j <= i; bidirectional keeps |i - j| < W.
+ *  softcap, scale  as in attn_decode.
+ *  out   device f16 [S, Hq, D].   lse_out  device f32 [S, Hq] or NULL.
+ *  D must be 64, 128 or 256.  Base addresses must be 16-byte aligned.
+ */
+attn_status attn_prefill(const void* q, const void* k, const void* v,
+                         int seq_len, int n_heads, int n_kv_heads, int head_dim,
+                         int causal, int window, float softcap, float scale,
+                         void* out, float* lse_out, void* stream);
+
+/*
+ * attn_decode_validate -- synchronous check of the device-side decode inputs:
+ * every kv_len[b] in [1, capacity] and every page id a sequence uses in
+ * [0, n_pages).  Launches one small kernel on stream and waits for it.
+ * Returns ATTN_OK, ATTN_EBOUNDS (bad page id or length > capacity; *bad_seq
+ * receives the first offending sequence if bad_seq != NULL) or ATTN_EINVAL
+ * (kv_len <= 0).  Not needed on the fast path: attn_decode never reads outside
+ * its buffers on such data (lengths are clamped to the capacity, a page id
+ * outside [0, n_pages) is replaced by page 0 and reported through
+ * attn_device_status), it only gives meaningless rows for those sequences.
+ */
+attn_status attn_decode_validate(const int32_t* kv_len, const int32_t* page_table,
+                                 int batch, int page_size, int max_pages_per_seq,
+                                 int n_pages, int max_kv, int* bad_seq, void* stream);
+
+/*
+ * attn_device_status -- synchronises stream, then reads and clears the
+ * library's device error word.  Returns ATTN_ETIMEOUT if a kernel abandoned a
+ * pipeline wait (its output is then invalid), ATTN_EBOUNDS if attn_decode met
+ * a page id outside the pool, else ATTN_OK.
+ */
+attn_status attn_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBATTN_ATTN_H */

@@ -1,0 +1,85 @@
+"""GPU parity of attn_prefill (tcgen05/TMEM tiled attention) against the oracle,
+through the C ABI: head dims 64/128/256, causal and bidirectional, windows,
+softcap, GQA, and sequence lengths that leave ragged 128-query and key tiles."""
+import numpy as np
+import pytest
+import torch
+
+import attention_split_kv_gb300 as attn
+import oracle
+import seeded_inputs as si
+from parity_util import assert_close, assert_lse_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    attn.build()
+    attn.load()
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    yield
+    assert attn.attn_device_status() == attn.ATTN_OK
+
+
+def _check(pc, what=""):
+    ref, ref_lse = oracle.prefill(pc)
+    g = pc.to("cuda")
+    lse = torch.empty((pc.seq_len, pc.n_heads), dtype=torch.float32, device="cuda")
+    out = attn.prefill(g, lse_out=lse)
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().numpy().reshape(ref.shape), ref, what=what)
+    assert_lse_close(lse.cpu().numpy().reshape(-1), ref_lse, what=what)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("S", [1, 100, 128, 300, 515])
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "bidir"])
+def test_prefill_plain(D, S, causal):
+    pc = si.make_prefill_case(S, 2, 1, D, seed=S + D, causal=causal)
+    _check(pc, what="S=%d D=%d causal=%s" % (S, D, causal))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal,window", [(True, 1), (True, 37), (True, 200), (False, 37), (False, 300)])
+def test_prefill_window(D, causal, window):
+    pc = si.make_prefill_case(400, 2, 2, D, seed=7 * window + D, causal=causal, window=window)
+    _check(pc, what="window %d causal=%s D=%d" % (window, causal, D))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("softcap", [5.0, 50.0])
+def test_prefill_softcap(D, softcap):
+    pc = si.make_prefill_case(333, 4, 2, D, seed=int(softcap) + D, causal=True, window=100,
+                              softcap=softcap, scale=1.0 / 16.0)
+    _check(pc, what="softcap %g D=%d" % (softcap, D))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (6, 3)])
+def test_prefill_gqa(Hq, Hkv):
+    pc = si.make_prefill_case(260, Hq, Hkv, 128, seed=Hq * 10 + Hkv, causal=True)
+    _check(pc, what="GQA %d/%d" % (Hq, Hkv))
+
+
+def test_prefill_large_logits_rescale_path():
+    # scores that grow along the keys force repeated lazy rescaling of O
+    pc = si.make_prefill_case(700, 2, 1, 64, seed=5, causal=False, scale=1.0)
+    k = pc.k.float()
+    ramp = torch.linspace(0.2, 3.0, pc.seq_len)[:, None, None]
+    pc.k = (k * ramp).to(torch.float16)
+    _check(pc, what="rescale path")
+
+
+def test_prefill_scale_zero_and_negative():
+    pc = si.make_prefill_case(150, 2, 1, 64, seed=6, causal=True, scale=0.0)
+    _check(pc, what="scale 0")
+    pc = si.make_prefill_case(150, 2, 1, 64, seed=7, causal=False, scale=-0.2)
+    _check(pc, what="negative scale")
+
+
+def test_prefill_is_deterministic():
+    pc = si.make_prefill_case(517, 4, 2, 128, seed=8, causal=True, window=64).to("cuda")
+    a = attn.prefill(pc).clone()
+    b = attn.prefill(pc)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
