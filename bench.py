@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention hot path through libattn's C ABI.
+
+One step = one call of each full-size seeded workload, which together cover
+every step of the path (page-table indirection, int8 dequant, GQA, softcap,
+masks, online softmax, PV, split combine, tensor-core prefill tiles):
+
+  vision_2304          bidirectional vision attention, S=2304, 16 heads, D=64   (headline)
+  paged_gqa_decode     B=32, 32q/8kv heads, D=128, kv_len ~ U[512, 8192], 16-token pages
+  swa_softcap_prefill  S=4096, 8q/4kv heads, D=256, causal, window 1024, softcap 50
+  int8_long_decode     B=16, 32q/8kv heads, D=128, kv_len 32768, int8 K/V + f16 scales
+
+The headline metric is the vision workload's TFLOP/s (algorithmic FLOPs
+4*S^2*D*H over the call's CUDA-event time); decode workloads report KV GB/s.
+Inputs are resident in HBM; L2 is flushed (256 MiB write) before every timed
+call, outside the timed events.  `e2e` repeats the headline through the same
+C-ABI call with pinned host buffers and the host<->device copies inside the
+timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the same workloads on its own GPU
+(independent replicas, no data-path collective) and rank 0 prints the line.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload instead (the only CPU implementation of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "vision_2304"
+METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
+WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode"]
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- algorithmic work
+def live_pairs(S, causal, window):
+    """Number of kept (query, key) pairs of one head (mask enumeration by rows)."""
+    total = 0
+    for i in range(S):
+        if causal:
+            lo = 0 if window <= 0 else max(0, i - window + 1)
+            hi = i
+        else:
+            lo = 0 if window <= 0 else max(0, i - window + 1)
+            hi = S - 1 if window <= 0 else min(S - 1, i + window - 1)
+        total += hi - lo + 1
+    return total
+
+
+def prefill_flops(case):
+    # QK^T and PV: 2 * D flops each per kept (query, key) pair and query head
+    return 4.0 * case.head_dim * live_pairs(case.seq_len, case.causal, case.window) * case.n_heads
+
+
+def decode_bytes(case):
+    """KV bytes a decode call must read once, plus q, out, kv_len and page table."""
+    esz = 1 if case.int8 else 2
+    per_tok = case.n_kv_heads * case.head_dim * esz * 2 + (case.n_kv_heads * 2 * 2 if case.int8 else 0)
+    kv = 0
+    pages = 0
+    for L in case.lens:
+        Le = min(L, case.window) if case.window > 0 else L
+        kv += Le * per_tok
+        if case.paged:
+            pages += (L + case.page_size - 1) // case.page_size
+    qo = 2 * case.batch * case.n_heads * case.head_dim * 2
+    return kv + qo + case.batch * 4 + pages * 4
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi SM clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        return self.summary(self.lines)
+
+    @staticmethod
+    def summary(lines):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed helpers
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value, world):
+    """Max of a host scalar over ranks (timing only; no data-path collective)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value, world):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample_rate(case, n_rows, seed=0):
+    """Time the oracle on n_rows sampled (query, head) rows of a prefill case.
+
+    Returns (TFLOP/s credited at the workload's per-row algorithmic FLOPs,
+    seconds, threads)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    rows = [(int(rng.integers(case.seq_len)), int(rng.integers(case.n_heads))) for _ in range(n_rows)]
+    per_row = prefill_flops(case) / (case.seq_len * case.n_heads)
+    t0 = time.perf_counter()
+    oracle.prefill(case, rows=rows)
+    dt = time.perf_counter() - t0
+    return per_row * n_rows / dt / 1e12, dt, oracle.max_threads()
+
+
+def cpu_baseline(case, target_s=12.0):
+    """Bounded oracle sample (about target_s seconds) of the headline workload."""
+    probe = 64
+    _, dt, _ = oracle_sample_rate(case, probe, seed=1)
+    n = int(min(case.seq_len * case.n_heads, max(probe, probe * target_s / max(dt, 1e-6))))
+    rate, dt, threads = oracle_sample_rate(case, n, seed=2)
+    return {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d (query, head) rows of %s, %.1f s" % (n, case.seq_len * case.n_heads,
+                                                                    HEADLINE, dt)}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 CPU oracle on bounded samples of the headline workload."""
+    if rank != 0:
+        return 0
+    import seeded_inputs as si
+    import oracle
+    oracle.build()
+    case = si.make_workload(HEADLINE, device="cpu")
+    probe_rate, probe_dt, _ = oracle_sample_rate(case, 32, seed=0)
+    budget_per_step = 150.0 / max(1, args.steps + args.warmup)
+    rows = int(max(16, min(case.seq_len * case.n_heads, 32 * budget_per_step / max(probe_dt, 1e-6))))
+    for w in range(args.warmup):
+        oracle_sample_rate(case, rows, seed=100 + w)
+    total_t, flops = 0.0, 0.0
+    per_row = prefill_flops(case) / (case.seq_len * case.n_heads)
+    threads = oracle.max_threads()
+    for k in range(args.steps):
+        _, dt, threads = oracle_sample_rate(case, rows, seed=1000 + k)
+        total_t += dt
+        flops += per_row * rows
+    value = flops / total_t / 1e12
+    line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) f16 inputs)",
+            "config": {"workload": HEADLINE, "seq_len": case.seq_len, "n_heads": case.n_heads,
+                       "head_dim": case.head_dim, "causal": False,
+                       "sample_rows_per_step": rows},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": "%d sampled (query, head) rows of %s per step" % (rows, HEADLINE)},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="libattn", choices=["libattn", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default=",".join(WORKLOAD_ORDER))
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    import attention_split_kv_gb300 as attn
+    import seeded_inputs as si
+    attn.build()
+    attn.load()
+    peaks = load_peaks()
+    names = [n for n in args.workloads.split(",") if n]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+
+    cases, runs, work = {}, {}, {}
+    for n in names:
+        c = si.make_workload(n, device="cuda")
+        cases[n] = c
+        if si.WORKLOADS[n]["kind"] == "decode":
+            ws = torch.empty(attn.attn_decode_workspace_size(c.batch, c.n_heads, c.n_kv_heads, c.head_dim,
+                                                             c.cap), dtype=torch.uint8, device=dev)
+            out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float16, device=dev)
+            runs[n] = (lambda c=c, ws=ws, out=out: attn.decode(c, out=out, workspace=ws))
+            work[n] = ("GB/s", decode_bytes(c), "hbm", 2)
+        else:
+            out = torch.empty_like(c.q)
+            runs[n] = (lambda c=c, out=out: attn.prefill(c, out=out))
+            work[n] = ("TFLOP/s", prefill_flops(c), "tensor", 1)
+    torch.cuda.synchronize()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def one_step(events=None):
+        for i, n in enumerate(names):
+            flush.fill_(float(i))
+            if events is not None:
+                events[n][0].record(stream)
+            runs[n]()
+            if events is not None:
+                events[n][1].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    evs = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        one_step(evs[k])
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = {n: sum(evs[k][n][0].elapsed_time(evs[k][n][1]) for k in range(args.steps)) / args.steps for n in names}
+    status = attn.attn_device_status()
+    # ---- e2e: headline through the same call with host buffers and copies timed
+    e2e = None
+    if HEADLINE in names:
+        c = cases[HEADLINE]
+        hq, hk, hv = (t.cpu().pin_memory() for t in (c.q, c.k, c.v))
+        hout = torch.empty(c.q.shape, dtype=torch.float16).pin_memory()
+        dq, dk, dv, dout = (torch.empty_like(t) for t in (c.q, c.k, c.v, c.q))
+        e2e_case = si.PrefillCase(q=dq, k=dk, v=dv, seq_len=c.seq_len, n_heads=c.n_heads,
+                                  n_kv_heads=c.n_kv_heads, head_dim=c.head_dim, causal=c.causal,
+                                  window=c.window, softcap=c.softcap, scale=c.scale)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            attn.prefill(e2e_case, out=dout)
+            hout.copy_(dout, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        nbytes_in = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        e2e = {"value": sum_over_ranks(work[HEADLINE][1], world) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": nbytes_in,
+               "d2h_bytes_per_step": hout.numel() * hout.element_size()}
+    clk = clocks.stop()
+
+    results = {}
+    for n in names:
+        unit, amount, bound, launches = work[n]
+        t_ms = max_over_ranks(ms[n], world)
+        total = sum_over_ranks(amount, world)
+        if unit == "GB/s":
+            value = total / (t_ms * 1e-3) / 1e9
+            per_gpu = amount / (ms[n] * 1e-3) / 1e9
+            peak = peaks["hbm_gbs"]
+        else:
+            value = total / (t_ms * 1e-3) / 1e12
+            per_gpu = amount / (ms[n] * 1e-3) / 1e12
+            peak = peaks["bf16_tflops"]
+        results[n] = {"value": value, "unit": unit, "ms": t_ms, "launches_per_call": launches,
+                      "roofline": {"bound": bound, "achieved": per_gpu, "peak": peak,
+                                   "unit": unit, "frac": per_gpu / peak, "traffic": None,
+                                   "peak_source": peaks["source"],
+                                   "scope": "whole call" if launches > 1 else "single kernel"}}
+    if rank != 0:
+        return 0
+    head = results.get(HEADLINE) or results[names[0]]
+    head_name = HEADLINE if HEADLINE in results else names[0]
+    hc = cases[head_name]
+    line = {
+        "metric": METRIC,
+        "value": head["value"],
+        "unit": head["unit"],
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sum(r["ms"] for r in results.values()),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded N(0,1) f16 inputs; int8 K/V encoded from them)",
+        "config": {"workload": head_name, "seq_len": hc.seq_len, "n_heads": hc.n_heads,
+                   "head_dim": hc.head_dim, "causal": bool(hc.causal),
+                   "step": "one call of each of " + ",".join(names),
+                   "l2": "flushed before every timed call (256 MiB write, outside the timed events)",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": dict(head["roofline"]),
+        "workloads": results,
+        "e2e": e2e,
+        "gpu_launches": sum(results[n]["launches_per_call"] for n in names) * args.steps,
+        "clocks": clk,
+        "device_status": "ok" if status == 0 else "error %d" % status,
+    }
+    line["roofline"]["kernel"] = "prefill_tc_kernel<64>" if head_name == HEADLINE else head_name
+    if world == 1 and not args.no_cpu_baseline and head_name == HEADLINE:
+        import oracle
+        oracle.build()
+        line["cpu_baseline"] = cpu_baseline(cases[HEADLINE].to("cpu"))
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

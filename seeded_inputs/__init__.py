@@ -297,6 +297,18 @@ WORKLOADS = {
                              window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
 }
 
+# Reduced cases of the same kernels for ncu captures (inputs still larger than
+# the 129 MB L2, a few hundred MB on the device).
+PROFILE_WORKLOADS = {
+    "int8_decode_profile": dict(kind="decode", seed=5, batch=16, n_heads=32, n_kv_heads=8, head_dim=128,
+                                lens=[4096] * 16, int8=True, page_size=0, window=0, softcap=0.0,
+                                scale=1.0 / math.sqrt(128.0)),
+    "paged_decode_profile": dict(kind="decode", seed=3, batch=32, n_heads=32, n_kv_heads=8,
+                                 head_dim=128, lens=(512, 8192), int8=False, page_size=16,
+                                 n_pages=None, window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
+}
+WORKLOADS.update(PROFILE_WORKLOADS)
+
 
 def make_workload(name: str, device: str = "cpu"):
     w = dict(WORKLOADS[name])
