@@ -19,7 +19,7 @@ __all__ = [
     "ATTN_KV_F16", "ATTN_KV_INT8", "AttnError", "AttnLibraryMissing",
     "lib_path", "load", "build", "exported_symbols",
     "attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-    "attn_prefill", "attn_decode_validate", "attn_device_status",
+    "attn_decode_noalloc", "attn_prefill", "attn_decode_validate", "attn_device_status",
     "decode", "prefill",
 ]
 
@@ -34,7 +34,7 @@ _lib = None
 
 # every entry point include/attn.h declares
 exported_symbols = ("attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-                    "attn_prefill", "attn_decode_validate", "attn_device_status")
+                    "attn_decode_noalloc", "attn_prefill", "attn_decode_validate", "attn_device_status")
 
 
 class AttnLibraryMissing(RuntimeError):
@@ -71,6 +71,8 @@ def load():
     lib.attn_decode_workspace_size.restype = SZ
     lib.attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, I, I, I, I, I, F, F, I, P, P, P, SZ, P]
     lib.attn_decode.restype = I
+    lib.attn_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, I, I, I, I, I, F, F, I, P, P, P]
+    lib.attn_decode_noalloc.restype = I
     lib.attn_prefill.argtypes = [P, P, P, I, I, I, I, I, I, F, F, P, P, P]
     lib.attn_prefill.restype = I
     lib.attn_decode_validate.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(ctypes.c_int), P]
@@ -124,6 +126,18 @@ def attn_decode(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_pe
                               int(n_kv_heads), int(head_dim), int(window), float(softcap), float(scale),
                               int(split_keys), _ptr(out), _ptr(lse_out), _ptr(workspace),
                               int(workspace_bytes), _stream(stream)))
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages,
+                        max_kv, k_scales, v_scales, kv_dtype, batch, n_heads, n_kv_heads, head_dim, window,
+                        softcap, scale, split_keys, out, lse_out, stream=None) -> None:
+    """attn_decode without a caller workspace: the library's fixed 16 MiB
+    device scratch array is used instead (for callers that cannot allocate)."""
+    _check(load().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(page_table),
+                                      int(page_size), int(max_pages_per_seq), int(n_pages), int(max_kv),
+                                      _ptr(k_scales), _ptr(v_scales), int(kv_dtype), int(batch), int(n_heads),
+                                      int(n_kv_heads), int(head_dim), int(window), float(softcap), float(scale),
+                                      int(split_keys), _ptr(out), _ptr(lse_out), _stream(stream)))
 
 
 def attn_prefill(q, k, v, seq_len, n_heads, n_kv_heads, head_dim, causal, window, softcap, scale,

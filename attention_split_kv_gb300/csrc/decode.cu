@@ -32,6 +32,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "attn_internal.h"
 #include "ptx.cuh"
 
@@ -732,3 +734,79 @@ attn_status launch_decode(const DecodeLaunch& L, const DecodePlan& plan) {
 }
 
 }  // namespace attn
+
+// ----------------------------------------------------------------------------
+// attn_decode_noalloc: attn_decode with its scratch memory taken from a fixed
+// array compiled into this library instead of from the caller.
+//
+// Some callers cannot hand the library a workspace: code hosted inside an
+// engine that owns every byte of device memory and exposes no allocator to
+// its plugins, or a latency-critical decode loop that must never call
+// cudaMalloc (which can synchronise the whole device).  For them the split
+// partials live in `g_decode_scratch`, a file-scope device array of
+// kNoAllocScratchBytes that every GPU loading this library keeps until the
+// process exits.
+//
+// The array's name means nothing to host code (it is a host-side shadow, not
+// a device address), so the device address is looked up once per device with
+// cudaGetSymbolAddress while that device is current, and passed to the
+// kernels like any workspace pointer.  That lookup happens inside the first
+// call on each device; make that first call before any stream capture.
+// Nothing in the scratch needs to start at zero: every byte the kernels read
+// is written earlier in the same call.  All calls share the one array, so two
+// calls whose kernels overlap on the GPU (different streams, no ordering)
+// race on it; order such calls on one stream.
+// ----------------------------------------------------------------------------
+namespace attn {
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB per device
+}  // namespace attn
+
+static __device__ __align__(256) unsigned char g_decode_scratch[attn::kNoAllocScratchBytes];
+
+namespace attn {
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};
+
+// Device address of g_decode_scratch on the current device (looked up once).
+attn_status scratch_for_current_device(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(ATTN_ECUDA, "attn_decode_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return set_error(ATTN_EUNSUPPORTED, "attn_decode_noalloc: device index %d above 63", dev);
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return set_error(ATTN_ECUDA, "attn_decode_noalloc: cudaGetSymbolAddress(scratch): %s",
+                             cudaGetErrorString(e));
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return ATTN_OK;
+}
+}  // namespace
+}  // namespace attn
+
+extern "C" attn_status attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* kv_len, const int32_t* page_table, int page_size,
+                                           int max_pages_per_seq, int n_pages, int max_kv, const void* k_scales,
+                                           const void* v_scales, attn_kv_dtype kv_dtype, int batch, int n_heads,
+                                           int n_kv_heads, int head_dim, int window, float softcap, float scale,
+                                           int split_keys, void* out, float* lse_out, void* stream) {
+    const size_t need = attn_decode_workspace_size(batch, n_heads, n_kv_heads, head_dim, max_kv, split_keys);
+    if (need > attn::kNoAllocScratchBytes)
+        return attn::set_error(ATTN_EUNSUPPORTED,
+                               "attn_decode_noalloc: these sizes need %zu bytes of scratch, above the library's "
+                               "fixed %zu (use attn_decode with a caller workspace, or a larger split_keys)",
+                               need, attn::kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    if (need > 0) {   // invalid sizes (need == 0) are reported by attn_decode below
+        const attn_status st = attn::scratch_for_current_device(&scratch);
+        if (st != ATTN_OK) return st;
+    }
+    return attn_decode(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages, max_kv,
+                       k_scales, v_scales, kv_dtype, batch, n_heads, n_kv_heads, head_dim, window, softcap, scale,
+                       split_keys, out, lse_out, scratch, scratch ? attn::kNoAllocScratchBytes : 0, stream);
+}

@@ -118,6 +118,34 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
+ * memory, so cannot supply a workspace: for example a plugin running inside
+ * an engine that owns all device memory and offers it no allocator, or a
+ * latency-critical decode loop that must never call cudaMalloc (a call that
+ * can synchronise the whole device).  The source pages have no counterpart of
+ * this entry point; it is an addition of this library.
+ *
+ * Arguments and results are those of attn_decode without workspace and
+ * workspace_bytes.  The split partials go to a fixed 16 MiB device array
+ * compiled into the library; every GPU that loads the library holds that
+ * array until the process exits.  Sizes whose attn_decode_workspace_size
+ * exceeds 16 MiB are rejected with ATTN_EUNSUPPORTED (a larger split_keys
+ * lowers the need).  Nothing is allocated and no allocating routine is
+ * called.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array and no part of it
+ * needs to start at zero; calls whose kernels overlap on the GPU (different
+ * streams without ordering) race on it, so order them on one stream.
+ */
+attn_status attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* kv_len, const int32_t* page_table,
+                                int page_size, int max_pages_per_seq, int n_pages, int max_kv,
+                                const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
+                                int batch, int n_heads, int n_kv_heads, int head_dim,
+                                int window, float softcap, float scale, int split_keys,
+                                void* out, float* lse_out, void* stream);
+
+/*
  * attn_prefill -- tiled prefill / vision attention of S tokens over themselves
  * on the tensor cores (tcgen05 + TMEM, operands staged by TMA).
  *
