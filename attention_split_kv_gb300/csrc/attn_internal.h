@@ -81,8 +81,10 @@ struct DecodeLaunch {
 struct DecodePlan {
     int GH;            // query heads handled together per kv head (1, 2 or 4)
     int HG;            // head groups per kv head: G / GH
-    int split;         // keys per split (multiple of the 16-key tile)
-    long max_items;    // upper bound of work items
+    int n_hb;          // head blocks: groups of up to 8 (kv head, head group) units
+    int nh_box;        // kv heads covered by one TMA box (the widest head block)
+    int split;         // keys per split (multiple of 16)
+    long max_items;    // upper bound of work items (sequence, head block, split)
     size_t off_lse, off_o, bytes;
 };
 bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys, DecodePlan* plan);

@@ -8,24 +8,27 @@
 // buffers; doppler run.js runLayerAttentionGPU: decode query at position
 // kvLen-1 and the sliding-window clamp).  The pages' decode kernels give one
 // workgroup per head and reduce with subgroup max/add; here the KV range of
-// each (sequence, kv head, head group) is cut into fixed-size splits so the
-// whole GPU streams the cache:
+// each sequence is cut into fixed-size splits so the whole GPU streams the
+// cache:
 //
-//   decode_split_kernel   persistent, one CTA per SM.  A producer warp streams
-//                         16-token K/V tiles (plus int8 scales) into a ring
-//                         of shared-memory slots with TMA, following the page
-//                         table; 7 consumer warps each take whole tiles and
-//                         keep an online softmax per query head.  Inside a
-//                         warp, 8 (or 16) lanes share one key: each lane holds
-//                         D/8 dims of all GH query heads of the group in
-//                         registers, so a K row is read once for the GH heads
+//   decode_split_kernel   persistent, one CTA of 8 warps per SM.  A work item
+//                         is (sequence, head block, split): a head block is up
+//                         to 8 (kv head, query-head group) units and warp w
+//                         owns unit w for the whole split.  Tiles of 16 tokens
+//                         (8 for D=256) of every kv head of the block are one
+//                         TMA box per tensor (per page when paged): tens of KB
+//                         contiguous in the cache, so a handful of copies keep
+//                         HBM busy.  Warp 0's lane 0 also issues those copies,
+//                         NSLOT-1 tiles ahead, into a ring of shared-memory
+//                         slots with full/empty mbarriers.  Inside a warp,
+//                         8 (16 for D=256) lanes share one key: each lane
+//                         holds D/8 dims of the GH query heads of its unit in
+//                         registers, so a K row is read once for GH heads
 //                         (GQA: q-head h reads kv-head h / G).  Partial dots
 //                         are reduce-scattered across the key's lanes with
 //                         warp shuffles; int8 codes become floats in registers
-//                         and the per-token scales are applied once per key.
-//                         At the end of a split the 7 warps merge their
-//                         (max, sum, o) states in shared memory and the split
-//                         writes (lse, o / l) to the workspace.
+//                         and per-token scales apply once per key.  At the end
+//                         of a split each warp writes (lse, o / l) of its unit.
 //   decode_combine_kernel merges the splits of each (sequence, head) with the
 //                         log-sum-exp rule and writes f16 output (+ lse).
 #include <cuda.h>
@@ -40,9 +43,8 @@
 namespace attn {
 namespace {
 
-constexpr int T = 16;                     // keys per tile (one ring slot)
-constexpr int NCW = 7;                    // consumer warps (+1 producer: 256 threads, 255 registers each)
-constexpr int kDecThreads = (NCW + 1) * 32;
+constexpr int NW = 8;                     // warps per CTA = units per head block
+constexpr int kDecThreads = NW * 32;
 constexpr int kSmemBudget = 226 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
@@ -54,29 +56,30 @@ struct DecCfg {
     static constexpr int LPK = (D == 256) ? 16 : 8;          // lanes sharing one key
     static constexpr int LOG_LPK = (LPK == 16) ? 4 : 3;
     static constexpr int KPS = 32 / LPK;                     // keys per warp step
+    static constexpr int T = (D == 256) ? 8 : 16;            // tokens per tile
     static constexpr int NSTEP = T / KPS;
     static constexpr int E = D / LPK;                        // elements per lane
     static constexpr int VB = (RB / LPK) < 16 ? (RB / LPK) : 16;   // bytes per vector load
     static constexpr int EV = VB / ESZ;                      // elements per vector
     static constexpr int NV = E / EV;                        // vectors per lane per row
     static constexpr int LOG_GH = (GH == 4) ? 2 : (GH == 2) ? 1 : 0;
-    static constexpr int SCALE_BYTES = I8 ? 256 : 0;         // per tensor per slot
-    static constexpr int SLOT = 2 * T * RB + 2 * SCALE_BYTES;
+    static constexpr int KV_BYTES = T * NW * RB;             // one K (or V) tile, up to 8 kv heads
+    static constexpr int SC_BYTES = I8 ? 256 : 0;            // one K (or V) scale tile
+    static constexpr int SLOT = 2 * KV_BYTES + 2 * SC_BYTES;
     static constexpr int OFF_PREFIX = 0;
     static constexpr int PREFIX_BYTES = ((kDecodeMaxBatch + 1) * 4 + 127) / 128 * 128;
-    static constexpr int OFF_MERGE = OFF_PREFIX + PREFIX_BYTES;
-    static constexpr int MERGE_BYTES = (NCW * GH * (D + 2) * 4 + 127) / 128 * 128;
-    static constexpr int OFF_MISC = OFF_MERGE + MERGE_BYTES;   // scan scratch (32 ints) + abort flag
+    static constexpr int OFF_MISC = OFF_PREFIX + PREFIX_BYTES;   // scan scratch (32 ints) + abort flag
     static constexpr int MISC_BYTES = 256;
     static constexpr int OFF_BARS = OFF_MISC + MISC_BYTES;
-    static constexpr int NSLOT_RAW = (kSmemBudget - OFF_BARS - 2 * 32 * 8 - 1024) / SLOT;
-    static constexpr int NSLOT = NSLOT_RAW > 32 ? 32 : NSLOT_RAW;
+    static constexpr int NSLOT_RAW = (kSmemBudget - OFF_BARS - 2 * 8 * 8 - 1024) / SLOT;
+    static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
     static constexpr int OFF_RING = ((OFF_BARS + 2 * NSLOT * 8) + 1023) / 1024 * 1024;
     static constexpr int SMEM_USED = OFF_RING + NSLOT * SLOT;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
-    static_assert(NSLOT >= 10, "ring too small");
+    static_assert(NSLOT >= 3, "ring too small");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(E % EV == 0 && E % 2 == 0, "lane layout");
+    static_assert(NSTEP * KPS == T, "tile layout");
 };
 
 struct DecArgs {
@@ -86,7 +89,7 @@ struct DecArgs {
     int32_t* ws_prefix;
     float* ws_lse;
     float* ws_o;
-    int B, Hq, Hkv, G, HG, split, cap_eff, window, P, R, max_pages, n_pages, paged;
+    int B, Hq, Hkv, G, HG, U, n_hb, nh_box, split, cap_eff, window, P, R, max_pages, n_pages, paged;
     float qscale;      // multiplies q: scale*log2e (no cap) or scale/c (cap)
     float cap_log2;    // c*log2e, 0 when the cap is off
     int* err;
@@ -100,18 +103,19 @@ __device__ __forceinline__ void seq_range(int L, int cap_eff, int W, int& start,
     start = (W > 0) ? max(0, L - W) : 0;
     end = L;
 }
-// Splits of a sequence: aligned to the tile so that tiles start on multiples
-// of 16 keys (and so on page boundaries for pages of >= 16 tokens).
+// Splits of a sequence: aligned to 16 tokens so that tiles start on multiples
+// of the tile (and so on page boundaries for pages of >= 16 tokens).
 __device__ __forceinline__ int seq_splits(int start, int end, int split) {
     if (end <= start) return 0;
-    const int a = (start / T) * T;
+    const int a = (start / 16) * 16;
     return (end - a + split - 1) / split;
 }
 
 struct Item {
-    int b, g, hg, ks, ke, start, ntile;
+    int b, hb, ks, ke, start, end, ntile;
 };
 
+template <int T>
 __device__ __forceinline__ Item decode_item(int it, const int* pref, const DecArgs& A) {
     int lo = 0, hi = A.B;   // largest b with pref[b] <= it
     while (hi - lo > 1) {
@@ -120,17 +124,13 @@ __device__ __forceinline__ Item decode_item(int it, const int* pref, const DecAr
     }
     Item r;
     r.b = lo;
-    int start, end;
-    seq_range(__ldg(&A.kv_len[lo]), A.cap_eff, A.window, start, end);
-    const int ns = seq_splits(start, end, A.split);
+    seq_range(__ldg(&A.kv_len[lo]), A.cap_eff, A.window, r.start, r.end);
+    const int ns = seq_splits(r.start, r.end, A.split);
     const int rem = it - pref[lo];
-    const int gh = rem / ns, s = rem - gh * ns;
-    r.g = gh / A.HG;
-    r.hg = gh - r.g * A.HG;
-    const int a = (start / T) * T;
-    r.ks = a + s * A.split;
-    r.ke = min(r.ks + A.split, end);
-    r.start = start;
+    r.hb = rem / ns;
+    const int s = rem - r.hb * ns;
+    r.ks = (r.start / 16) * 16 + s * A.split;
+    r.ke = min(r.ks + A.split, r.end);
     r.ntile = (r.ke - r.ks + T - 1) / T;
     return r;
 }
@@ -146,7 +146,7 @@ __device__ void build_prefix(const DecArgs& A, int* pref, int* scratch) {
         if (b < A.B) {
             int start, end;
             seq_range(__ldg(&A.kv_len[b]), A.cap_eff, A.window, start, end);
-            v = A.Hkv * A.HG * seq_splits(start, end, A.split);
+            v = A.n_hb * seq_splits(start, end, A.split);
         }
         int x = v;
 #pragma unroll
@@ -216,9 +216,9 @@ __device__ __forceinline__ void load_row_slice(const uint8_t* row, int c, float2
         } else {
             // int8 code u -> float: bytes biased to unsigned, placed in the low
             // mantissa bits of 2^23, then the bias 2^23 + 128 is subtracted.
-            constexpr int NW = C::VB / 4;
-            uint32_t ws[NW];
-            if constexpr (NW == 4) {
+            constexpr int NWD = C::VB / 4;
+            uint32_t ws[NWD];
+            if constexpr (NWD == 4) {
                 const uint4 w = *reinterpret_cast<const uint4*>(src);
                 ws[0] = w.x; ws[1] = w.y; ws[2] = w.z; ws[3] = w.w;
             } else {
@@ -227,7 +227,7 @@ __device__ __forceinline__ void load_row_slice(const uint8_t* row, int c, float2
             }
             const float2 bias = make_float2(-8388736.0f, -8388736.0f);
 #pragma unroll
-            for (int i = 0; i < NW; ++i) {
+            for (int i = 0; i < NWD; ++i) {
                 const uint32_t u = ws[i] ^ 0x80808080u;
                 const float2 lo = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u)),
                                               __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541u)));
@@ -246,11 +246,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
                     const DecArgs A) {
     using C = DecCfg<D, I8, GH>;
-    constexpr int NSLOT = C::NSLOT, LPK = C::LPK, E = C::E;
+    constexpr int NSLOT = C::NSLOT, LPK = C::LPK, E = C::E, T = C::T;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int* pref = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
-    float* mb = reinterpret_cast<float*>(smem + C::OFF_MERGE);
     int* scratch = reinterpret_cast<int*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 128);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
@@ -262,7 +261,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), NW);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -272,114 +271,119 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     if (blockIdx.x == 0) {
         for (int b = threadIdx.x; b <= A.B; b += blockDim.x) A.ws_prefix[b] = pref[b];
     }
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        if (I8) {
+            tma_prefetch_desc(&tm_ks);
+            tma_prefetch_desc(&tm_vs);
+        }
+    }
 
-    if (warp == NCW) {
-        // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            if (I8) {
-                tma_prefetch_desc(&tm_ks);
-                tma_prefetch_desc(&tm_vs);
+    // ------------------------------------------------------------------ producer state (warp 0)
+    // Tiles are issued in the order the CTA consumes them; `issued` counts
+    // them, (p_it, p_i) is the next tile to issue.
+    uint32_t issued = 0;
+    int p_it = blockIdx.x, p_i = 0;
+    Item p_item;
+    if (warp == 0 && p_it < total) p_item = decode_item<T>(p_it, pref, A);
+    int cache_b = -1, cache_base = -1, pid = -1;
+    const int NB = T / A.R;                                   // boxes per tile per tensor
+    const uint32_t box_kv = A.R * A.nh_box * C::RB;           // bytes of one K (or V) box
+    const uint32_t box_sc = A.R * A.nh_box * 2;               // bytes of one scale box
+    const uint32_t sbb = (box_sc + 127) / 128 * 128;          // scale boxes start 128-byte aligned
+    bool ok = true;
+
+    // Issue tiles until `target` (a consumption count) is covered.  Whole warp 0.
+    auto produce_until = [&](uint32_t target) {
+        while (ok && issued <= target && p_it < total) {
+            const int t0 = p_item.ks + p_i * T;
+            const int slot = issued % NSLOT;
+            const int g0 = (p_item.hb * NW) / A.HG;
+            int pi0 = 0, cb = 0;
+            if (A.paged) {
+                pi0 = t0 / A.P;
+                cb = pi0 & ~31;
+                if (p_item.b != cache_b || cb != cache_base) {
+                    const int idx = cb + lane;
+                    pid = idx < A.max_pages ? __ldg(&A.page_table[(size_t)p_item.b * A.max_pages + idx]) : -1;
+                    cache_b = p_item.b;
+                    cache_base = cb;
+                }
             }
-        }
-        const int NB = T / A.R;          // boxes per tile per tensor
-        uint32_t gt = 0;
-        int cache_b = -1, cache_base = -1, pid = -1;
-        bool ok = true;
-        for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-            const Item I = decode_item(it, pref, A);
-            int start, end;
-            seq_range(__ldg(&A.kv_len[I.b]), A.cap_eff, A.window, start, end);
-            for (int i = 0; i < I.ntile; ++i, ++gt) {
-                const int t0 = I.ks + i * T;
-                const int slot = gt % NSLOT;
-                int pi0 = 0, cb = 0;
+            int good = 1;
+            if (lane == 0 && issued >= (uint32_t)NSLOT)
+                good = mbar_wait(empty_bar(slot), ((issued / NSLOT) - 1) & 1, abort_flag, A.err, kErrTimeoutSlot);
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) { ok = false; break; }
+            const uint32_t sb = ring + slot * C::SLOT;
+            int nbox = 1;
+            if (A.paged) {
+                nbox = 0;
+                for (int r = 0; r < NB; ++r)
+                    if ((pi0 + r) * A.P < p_item.end) nbox = r + 1;
+            }
+            const uint32_t bytes = nbox * (2 * box_kv + (I8 ? 2 * box_sc : 0));
+            if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), bytes);
+            for (int r = 0; r < nbox; ++r) {
+                int page = p_item.b, row = t0;
                 if (A.paged) {
-                    pi0 = t0 / A.P;
-                    cb = pi0 & ~31;
-                    if (I.b != cache_b || cb != cache_base) {
-                        const int idx = cb + lane;
-                        pid = idx < A.max_pages ? __ldg(&A.page_table[(size_t)I.b * A.max_pages + idx]) : -1;
-                        cache_b = I.b;
-                        cache_base = cb;
+                    page = __shfl_sync(0xffffffffu, pid, pi0 + r - cb);
+                    if (page < 0 || page >= A.n_pages) {
+                        // a page id outside the pool: read page 0 instead and report it
+                        if (lane == 0) atomicExch(A.err, kErrBadPage);
+                        page = 0;
+                    }
+                    row = (A.P >= T) ? (t0 % A.P) : 0;
+                }
+                if (lane == 0) {
+                    tma_load_4d(sb + r * box_kv, &tm_k, full_bar(slot), 0, g0, row, page);
+                    tma_load_4d(sb + C::KV_BYTES + r * box_kv, &tm_v, full_bar(slot), 0, g0, row, page);
+                    if (I8) {
+                        tma_load_3d(sb + 2 * C::KV_BYTES + r * sbb, &tm_ks, full_bar(slot), row, g0, page);
+                        tma_load_3d(sb + 2 * C::KV_BYTES + C::SC_BYTES + r * sbb, &tm_vs, full_bar(slot), row, g0, page);
                     }
                 }
-                int good = 1;
-                if (lane == 0 && gt >= (uint32_t)NSLOT)
-                    good = mbar_wait(empty_bar(slot), ((gt / NSLOT) - 1) & 1, abort_flag, A.err, kErrTimeoutSlot);
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) { ok = false; break; }
-                const uint32_t sb = ring + slot * C::SLOT;
-                const int row0 = (A.paged && A.P >= T) ? (t0 % A.P) : (A.paged ? 0 : t0);
-                uint32_t bytes = 0;
-                // count the boxes first (lane 0 arms the barrier before any copy lands)
-                int nbox = 0;
-                if (!A.paged) {
-                    nbox = 1;
-                } else {
-                    for (int r = 0; r < NB; ++r)
-                        if ((pi0 + r) * A.P < end) nbox = r + 1;
-                }
-                bytes = nbox * A.R * (2 * C::RB + (I8 ? 4 : 0));
-                if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), bytes);
-                for (int r = 0; r < nbox; ++r) {
-                    int page = I.b;
-                    if (A.paged) {
-                        page = __shfl_sync(0xffffffffu, pid, pi0 + r - cb);
-                        if (page < 0 || page >= A.n_pages) {
-                            // a page id outside the pool: read page 0 instead and report it
-                            if (lane == 0) atomicExch(A.err, kErrBadPage);
-                            page = 0;
-                        }
-                    }
-                    if (lane == 0) {
-                        const int rr = row0;
-                        tma_load_4d(sb + r * A.R * C::RB, &tm_k, full_bar(slot), 0, I.g, rr, page);
-                        tma_load_4d(sb + T * C::RB + r * A.R * C::RB, &tm_v, full_bar(slot), 0, I.g, rr, page);
-                        if (I8) {
-                            tma_load_3d(sb + 2 * T * C::RB + r * 128, &tm_ks, full_bar(slot), rr, I.g, page);
-                            tma_load_3d(sb + 2 * T * C::RB + C::SCALE_BYTES + r * 128, &tm_vs, full_bar(slot), rr,
-                                        I.g, page);
-                        }
-                    }
-                }
-                __syncwarp();
+            }
+            __syncwarp();
+            ++issued;
+            if (++p_i == p_item.ntile) {
+                p_i = 0;
+                p_it += gridDim.x;
+                if (p_it < total) p_item = decode_item<T>(p_it, pref, A);
             }
         }
-        if (!ok && lane == 0) {
-            // let copies in flight land before shared memory is released
-            volatile int never = 0;
-            const uint32_t first = gt > (uint32_t)NSLOT ? gt - NSLOT : 0;
-            for (uint32_t x = first; x < gt; ++x)
-                mbar_wait(full_bar(x % NSLOT), (x / NSLOT) & 1, &never, A.err, kErrTimeoutLoad);
-        }
-    } else {
-        // ---------------------------------------------------------------- consumers
-        const int c = lane & (LPK - 1);          // position inside the key's lane group
-        const int kk = lane >> C::LOG_LPK;       // key of the step handled by this group
-        const int grp = lane & ~(LPK - 1);
-        // reduce-scatter bookkeeping: slot s of this lane holds head s ^ rot
-        int rot = 0;
+    };
+
+    // ------------------------------------------------------------------ consumers (all warps)
+    const int c = lane & (LPK - 1);          // position inside the key's lane group
+    const int kk = lane >> C::LOG_LPK;       // key of the step handled by this group
+    const int grp = lane & ~(LPK - 1);
+    // reduce-scatter bookkeeping: slot s of this lane holds head s ^ rot
+    int rot = 0;
 #pragma unroll
-        for (int k = 0; k < C::LOG_GH; ++k) rot |= ((c >> (C::LOG_LPK - 1 - k)) & 1) << (C::LOG_GH - 1 - k);
-        int src_lane[GH];   // a lane of this group holding head h after the scatter
+    for (int k = 0; k < C::LOG_GH; ++k) rot |= ((c >> (C::LOG_LPK - 1 - k)) & 1) << (C::LOG_GH - 1 - k);
+    int src_lane[GH];   // a lane of this group holding head h after the scatter
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
-            int cl = 0;
+    for (int h = 0; h < GH; ++h) {
+        int cl = 0;
 #pragma unroll
-            for (int k = 0; k < C::LOG_GH; ++k) cl |= ((h >> (C::LOG_GH - 1 - k)) & 1) << (C::LOG_LPK - 1 - k);
-            src_lane[h] = grp | cl;
-        }
-        uint32_t gt_base = 0;
-        bool ok = true;
-        for (int it = blockIdx.x; it < total; it += gridDim.x) {
-            const Item I = decode_item(it, pref, A);
-            // queries of the GH heads, pre-scaled, in this lane's dims and slot order
-            float2 q2[GH][E / 2];
+        for (int k = 0; k < C::LOG_GH; ++k) cl |= ((h >> (C::LOG_GH - 1 - k)) & 1) << (C::LOG_LPK - 1 - k);
+        src_lane[h] = grp | cl;
+    }
+    uint32_t gcons = 0;
+    for (int it = blockIdx.x; it < total; it += gridDim.x) {
+        const Item I = decode_item<T>(it, pref, A);
+        const int u = I.hb * NW + warp;
+        const bool active = u < A.U;
+        const int g = active ? u / A.HG : 0;
+        const int hg = active ? u - g * A.HG : 0;
+        const int hl = g - (I.hb * NW) / A.HG;   // this unit's kv head inside the tile
+        float2 q2[GH][E / 2];
+        if (active) {
 #pragma unroll
             for (int s = 0; s < GH; ++s) {
-                const int head = I.g * A.G + I.hg * GH + (s ^ rot);
+                const int head = g * A.G + hg * GH + (s ^ rot);
                 const __half* qrow = A.q + ((size_t)I.b * A.Hq + head) * D;
 #pragma unroll
                 for (int v = 0; v < C::NV; ++v)
@@ -390,33 +394,36 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                         q2[s][(v * C::EV + e) / 2] = make_float2(f.x * A.qscale, f.y * A.qscale);
                     }
             }
-            float2 o2[GH][E / 2];
+        }
+        float2 o2[GH][E / 2];
 #pragma unroll
-            for (int h = 0; h < GH; ++h)
+        for (int h = 0; h < GH; ++h)
 #pragma unroll
-                for (int j = 0; j < E / 2; ++j) o2[h][j] = make_float2(0.f, 0.f);
-            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < E / 2; ++j) o2[h][j] = make_float2(0.f, 0.f);
+        float m = -INFINITY, l = 0.f;
 
-            for (int i = warp; i < I.ntile; i += NCW) {
-                const uint32_t gt = gt_base + i;
-                const int slot = gt % NSLOT;
-                bool got = ok && mbar_wait(full_bar(slot), (gt / NSLOT) & 1, abort_flag, A.err, kErrTimeoutLoad);
-                got = __all_sync(0xffffffffu, got);   // keep the warp converged for the shuffles below
-                if (!got) { ok = false; continue; }
+        for (int i = 0; i < I.ntile; ++i, ++gcons) {
+            if (warp == 0) produce_until(gcons + NSLOT - 1);
+            const int slot = gcons % NSLOT;
+            bool got = ok && mbar_wait(full_bar(slot), (gcons / NSLOT) & 1, abort_flag, A.err, kErrTimeoutLoad);
+            got = __all_sync(0xffffffffu, got);   // keep the warp converged for the shuffles below
+            if (!got) { ok = false; continue; }
+            if (active) {
                 const int t0 = I.ks + i * T;
                 const int v_lo = max(I.start - t0, 0);
                 const int v_hi = min(I.ke - t0, T);
                 const uint8_t* kt = smem + C::OFF_RING + slot * C::SLOT;
-                const uint8_t* vt = kt + T * C::RB;
-                const __half* kst = reinterpret_cast<const __half*>(kt + 2 * T * C::RB);
-                const __half* vst = reinterpret_cast<const __half*>(kt + 2 * T * C::RB + C::SCALE_BYTES);
+                const uint8_t* vt = kt + C::KV_BYTES;
+                const __half* kst = reinterpret_cast<const __half*>(kt + 2 * C::KV_BYTES);
+                const __half* vst = reinterpret_cast<const __half*>(kt + 2 * C::KV_BYTES + C::SC_BYTES);
+                const int sc_off = hl * A.R;   // this head's scales inside a scale box (elements)
 
                 float tsc[C::NSTEP];
 #pragma unroll
                 for (int st = 0; st < C::NSTEP; ++st) {
                     const int key = st * C::KPS + kk;
                     float2 kx[E / 2];
-                    load_row_slice<D, I8, GH>(kt + key * C::RB, c, kx);
+                    load_row_slice<D, I8, GH>(kt + (key * A.nh_box + hl) * C::RB, c, kx);
                     float acc[GH];
 #pragma unroll
                     for (int s = 0; s < GH; ++s) {
@@ -437,7 +444,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     for (int dist = LPK >> (C::LOG_GH + 1); dist >= 1; dist >>= 1)
                         acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], dist);
                     float t = acc[0];
-                    if (I8) t *= __half2float(kst[(key / A.R) * 64 + (key % A.R)]);
+                    if (I8) t *= __half2float(kst[(key / A.R) * (sbb / 2) + sc_off + (key % A.R)]);
                     if (A.cap_log2 > 0.f) t = A.cap_log2 * tanh_abs_accurate(t);
                     tsc[st] = (key >= v_lo && key < v_hi) ? t : -INFINITY;
                 }
@@ -470,7 +477,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     if (I8) {
                         const int key = st * C::KPS + kk;
                         const bool valid = key >= v_lo && key < v_hi;
-                        pv[st] = valid ? p * __half2float(vst[(key / A.R) * 64 + (key % A.R)]) : 0.f;
+                        pv[st] = valid ? p * __half2float(vst[(key / A.R) * (sbb / 2) + sc_off + (key % A.R)]) : 0.f;
                     }
                 }
 #pragma unroll
@@ -481,7 +488,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     for (int h = 0; h < GH; ++h) pg[h] = __shfl_sync(0xffffffffu, pv[st], src_lane[h]);
                     if (key >= v_lo && key < v_hi) {
                         float2 vx[E / 2];
-                        load_row_slice<D, I8, GH>(vt + key * C::RB, c, vx);
+                        load_row_slice<D, I8, GH>(vt + (key * A.nh_box + hl) * C::RB, c, vx);
 #pragma unroll
                         for (int h = 0; h < GH; ++h) {
                             const float2 pp = make_float2(pg[h], pg[h]);
@@ -490,65 +497,49 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                         }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(slot));
             }
-            gt_base += I.ntile;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(slot));
+        }
+        if (!active) continue;
 
-            // ---- merge: lanes of a key group -> group 0, then warps via shared memory
+        // ---- end of the split: key groups -> group 0, then (lse, o / l) of each head
 #pragma unroll
-            for (int dist = LPK; dist < 32; dist <<= 1) {
+        for (int dist = LPK; dist < 32; dist <<= 1) {
 #pragma unroll
-                for (int h = 0; h < GH; ++h)
+            for (int h = 0; h < GH; ++h)
 #pragma unroll
-                    for (int j = 0; j < E / 2; ++j) {
-                        o2[h][j].x += __shfl_xor_sync(0xffffffffu, o2[h][j].x, dist);
-                        o2[h][j].y += __shfl_xor_sync(0xffffffffu, o2[h][j].y, dist);
-                    }
-                l += __shfl_xor_sync(0xffffffffu, l, dist);
-            }
-            float* mb_m = mb;                         // [NCW][GH]
-            float* mb_l = mb + NCW * GH;              // [NCW][GH]
-            float* mb_o = mb + 2 * NCW * GH;          // [NCW][GH][D]
+                for (int j = 0; j < E / 2; ++j) {
+                    o2[h][j].x += __shfl_xor_sync(0xffffffffu, o2[h][j].x, dist);
+                    o2[h][j].y += __shfl_xor_sync(0xffffffffu, o2[h][j].y, dist);
+                }
+            l += __shfl_xor_sync(0xffffffffu, l, dist);
+        }
+        const size_t prow = ((size_t)it * NW + warp) * GH;   // this unit's partial rows
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            const float lh = __shfl_sync(0xffffffffu, l, src_lane[h]);
+            const float mh = __shfl_sync(0xffffffffu, m, src_lane[h]);
+            const float inv = lh > 0.f ? 1.0f / lh : 0.f;
             if (lane < LPK) {
 #pragma unroll
-                for (int h = 0; h < GH; ++h)
+                for (int v = 0; v < C::NV; ++v)
 #pragma unroll
-                    for (int v = 0; v < C::NV; ++v)
-#pragma unroll
-                        for (int e = 0; e < C::EV; e += 2) {
-                            const int dim = (v * LPK + c) * C::EV + e;
-                            *reinterpret_cast<float2*>(&mb_o[(warp * GH + h) * D + dim]) = o2[h][(v * C::EV + e) / 2];
-                        }
-                if ((c & ((LPK >> C::LOG_GH) - 1)) == 0) {   // one writer per head
-                    mb_m[warp * GH + rot] = m;
-                    mb_l[warp * GH + rot] = l;
-                }
-            }
-            named_bar_sync(1, NCW * 32);
-            for (int idx = threadIdx.x; idx < GH * D; idx += NCW * 32) {
-                const int h = idx / D, d = idx - h * D;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < NCW; ++w) M = fmaxf(M, mb_m[w * GH + h]);
-                float wsum = 0.f, acc = 0.f;
-                if (M > -INFINITY) {
-#pragma unroll
-                    for (int w = 0; w < NCW; ++w) {
-                        const float mw = mb_m[w * GH + h];
-                        if (mw > -INFINITY) {
-                            const float f = ex2_approx(mw - M);
-                            wsum += mb_l[w * GH + h] * f;
-                            acc += mb_o[(w * GH + h) * D + d] * f;
-                        }
+                    for (int e = 0; e < C::EV; e += 2) {
+                        const int dim = (v * LPK + c) * C::EV + e;
+                        const float2 ov = o2[h][(v * C::EV + e) / 2];
+                        *reinterpret_cast<float2*>(&A.ws_o[(prow + h) * D + dim]) = make_float2(ov.x * inv, ov.y * inv);
                     }
-                }
-                const size_t row = (size_t)it * GH + h;
-                A.ws_o[row * D + d] = wsum > 0.f ? acc / wsum : 0.f;
-                if (d == 0) A.ws_lse[row] = wsum > 0.f ? M + __log2f(wsum) : -INFINITY;
             }
-            named_bar_sync(1, NCW * 32);
+            if (lane == 0) A.ws_lse[prow + h] = lh > 0.f ? mh + __log2f(lh) : -INFINITY;
         }
+    }
+    if (warp == 0 && !ok && lane == 0) {
+        // let copies in flight land before shared memory is released
+        volatile int never = 0;
+        const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
+        for (uint32_t x = first; x < issued; ++x)
+            mbar_wait(full_bar(x % NSLOT), (x / NSLOT) & 1, &never, A.err, kErrTimeoutLoad);
     }
 }
 
@@ -557,20 +548,21 @@ template <int D>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const int32_t* __restrict__ kv_len, const int32_t* __restrict__ ws_prefix,
                       const float* __restrict__ ws_lse, const float* __restrict__ ws_o, __half* __restrict__ out,
-                      float* __restrict__ lse_out, int B, int Hq, int Hkv, int G, int GH, int HG, int split,
-                      int cap_eff, int window) {
+                      float* __restrict__ lse_out, int B, int Hq, int G, int GH, int HG, int split, int cap_eff,
+                      int window) {
     constexpr int DPL = D / 32;   // dims per lane
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (gw >= B * Hq) return;
     const int b = gw / Hq, h = gw - b * Hq;
     const int g = h / G, r = h - g * G, hg = r / GH, hs = r - hg * GH;
+    const int u = g * HG + hg, hb = u / NW, w = u - hb * NW;
     int start, end;
     seq_range(kv_len[b], cap_eff, window, start, end);
     const int ns = seq_splits(start, end, split);
-    const int item0 = ws_prefix[b] + (g * HG + hg) * ns;
+    const int item0 = ws_prefix[b] + hb * ns;
     float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, ws_lse[(size_t)(item0 + s) * GH + hs]);
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, ws_lse[((size_t)(item0 + s) * NW + w) * GH + hs]);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float acc[DPL];
@@ -579,14 +571,14 @@ decode_combine_kernel(const int32_t* __restrict__ kv_len, const int32_t* __restr
     float wsum = 0.f;
     if (M > -INFINITY) {
         for (int s = 0; s < ns; ++s) {
-            const size_t row = (size_t)(item0 + s) * GH + hs;
+            const size_t row = ((size_t)(item0 + s) * NW + w) * GH + hs;
             const float ls = ws_lse[row];
             if (ls == -INFINITY) continue;
-            const float w = ex2_approx(ls - M);
-            wsum += w;
+            const float wt = ex2_approx(ls - M);
+            wsum += wt;
             const float* src = ws_o + row * D + lane * DPL;
 #pragma unroll
-            for (int i = 0; i < DPL; ++i) acc[i] += w * src[i];
+            for (int i = 0; i < DPL; ++i) acc[i] += wt * src[i];
         }
     }
     const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
@@ -603,12 +595,13 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
     const int esz = I8 ? 1 : 2;
     const CUtensorMapDataType kvt = I8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const bool paged = L.page_table != nullptr;
-    const int R = paged ? (L.page_size < T ? L.page_size : T) : T;
+    const int R = paged ? (L.page_size < C::T ? L.page_size : C::T) : C::T;
     CUtensorMap tk, tv, tks, tvs;
     attn_status st;
     {
+        // [pages or B][rows][Hkv][D]: boxes of (D, nh_box heads, R rows, 1)
         uint64_t dims[4], strides[3];
-        uint32_t box[4] = {(uint32_t)D, 1u, (uint32_t)R, 1u};
+        uint32_t box[4] = {(uint32_t)D, (uint32_t)plan.nh_box, (uint32_t)R, 1u};
         dims[0] = D;
         dims[1] = L.Hkv;
         dims[2] = paged ? L.page_size : L.max_kv;
@@ -620,8 +613,9 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
         if ((st = encode_tmap_plain(&tv, L.v, kvt, 4, dims, strides, box)) != ATTN_OK) return st;
     }
     if (I8) {
+        // [pages or B][Hkv][rows]: boxes of (R rows, nh_box heads, 1)
         uint64_t dims[3], strides[2];
-        uint32_t box[3] = {(uint32_t)R, 1u, 1u};
+        uint32_t box[3] = {(uint32_t)R, (uint32_t)plan.nh_box, 1u};
         dims[0] = paged ? L.page_size : L.max_kv;
         dims[1] = L.Hkv;
         dims[2] = paged ? L.n_pages : L.B;
@@ -658,6 +652,9 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
     a.Hkv = L.Hkv;
     a.G = L.Hq / L.Hkv;
     a.HG = plan.HG;
+    a.U = L.Hkv * plan.HG;
+    a.n_hb = plan.n_hb;
+    a.nh_box = plan.nh_box;
     a.split = plan.split;
     a.cap_eff = cap_layout < L.max_kv ? cap_layout : L.max_kv;
     a.window = L.window;
@@ -678,8 +675,8 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode split launch failed: %s", cudaGetErrorString(e));
     const int nwarps = L.B * L.Hq;
     decode_combine_kernel<D><<<(nwarps + 3) / 4, 128, 0, L.stream>>>(
-        L.kv_len, a.ws_prefix, a.ws_lse, a.ws_o, static_cast<__half*>(L.out), L.lse, L.B, L.Hq, L.Hkv, a.G, GH,
-        plan.HG, plan.split, a.cap_eff, L.window);
+        L.kv_len, a.ws_prefix, a.ws_lse, a.ws_o, static_cast<__half*>(L.out), L.lse, L.B, L.Hq, a.G, GH, plan.HG,
+        plan.split, a.cap_eff, L.window);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode combine launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
@@ -702,24 +699,34 @@ bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys,
     const int G = Hq / Hkv;
     plan->GH = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
     plan->HG = G / plan->GH;
-    const long units = (long)B * Hkv * plan->HG;
+    const int U = Hkv * plan->HG;                  // (kv head, head group) units
+    plan->n_hb = (U + NW - 1) / NW;                // head blocks of up to 8 units
+    int nh = 1;
+    for (int hb = 0; hb < plan->n_hb; ++hb) {
+        const int u0 = hb * NW, u1 = (u0 + NW < U ? u0 + NW : U) - 1;
+        const int span = u1 / plan->HG - u0 / plan->HG + 1;
+        if (span > nh) nh = span;
+    }
+    plan->nh_box = nh;                             // kv heads one TMA box covers
+    const long units = (long)B * plan->n_hb;
     int split = split_keys;
     if (split == 0) {
-        // aim at ~2048 work items for the longest sequences
-        long want = (units * (long)max_kv + 2047) / 2048;
-        long p = 256;
-        while (p < want && p < 4096) p <<= 1;
+        // aim at ~1024 work items of (sequence, head block, split) for the longest sequences
+        long want = (units * (long)max_kv + 1023) / 1024;
+        long p = 64;
+        while (p < want && p < 8192) p <<= 1;
         split = (int)p;
     }
-    if (split % T != 0) return false;
+    if (split % 16 != 0) return false;
     plan->split = split;
-    // +1 split: tile alignment of a window start can add one partial split
+    // +1 split: aligning a window start down to the tile can add one partial split
     plan->max_items = units * ((max_kv + split - 1) / split + 1);
+    const size_t rows = (size_t)plan->max_items * NW * plan->GH;   // (item, warp, head) partial rows
     size_t off = ((size_t)(B + 1) * 4 + 255) / 256 * 256;
     plan->off_lse = off;
-    off += ((size_t)plan->max_items * plan->GH * 4 + 255) / 256 * 256;
+    off += (rows * 4 + 255) / 256 * 256;
     plan->off_o = off;
-    off += (size_t)plan->max_items * plan->GH * D * 4;
+    off += rows * D * 4;
     plan->bytes = off;
     return true;
 }

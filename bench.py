@@ -92,6 +92,16 @@ def decode_bytes(case):
     return kv + qo + case.batch * 4 + pages * 4
 
 
+def workload_config(case):
+    if hasattr(case, "seq_len"):
+        return {"seq_len": case.seq_len, "n_heads": case.n_heads, "n_kv_heads": case.n_kv_heads,
+                "head_dim": case.head_dim, "causal": bool(case.causal), "window": case.window,
+                "softcap": case.softcap}
+    return {"global_batch": case.batch, "n_heads": case.n_heads, "n_kv_heads": case.n_kv_heads,
+            "head_dim": case.head_dim, "kv_len_min": min(case.lens), "kv_len_max": max(case.lens),
+            "kv_dtype": "int8" if case.int8 else "f16", "page_size": case.page_size}
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi SM clock / throttle sampling during the timed region."""
@@ -397,8 +407,7 @@ def main(argv=None):
         "vs_baseline": None,
         "dtype": "f16",
         "data": "synthetic (seeded N(0,1) f16 inputs; int8 K/V encoded from them)",
-        "config": {"workload": head_name, "seq_len": hc.seq_len, "n_heads": hc.n_heads,
-                   "head_dim": hc.head_dim, "causal": bool(hc.causal),
+        "config": {"workload": head_name, **workload_config(hc),
                    "step": "one call of each of " + ",".join(names),
                    "l2": "flushed before every timed call (256 MiB write, outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
