@@ -38,7 +38,10 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 template <int D>
 struct PrefillCfg {
     static constexpr int NCH = D / 64;                   // 64-element (128-byte) chunks of D
-    static constexpr int BN = (D == 256) ? 64 : 128;     // keys per tile
+    // D=64 runs two CTAs per SM (64-key tiles, 256 TMEM columns each) so that
+    // two softmax warpgroups share every SM; D=128/256 run one CTA per SM.
+    static constexpr int CTAS_PER_SM = (D == 64) ? 2 : 1;
+    static constexpr int BN = (D == 128) ? 128 : 64;     // keys per tile
     static constexpr int STAGES = (D == 64) ? 3 : 2;     // K/V ring depth
     static constexpr int PCH = BN / 64;                  // 64-key chunks of a P row
     static constexpr uint32_t Q_BYTES = NCH * BM * 128;
@@ -55,13 +58,16 @@ struct PrefillCfg {
     static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // slack for 1024-byte alignment
-    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TMEM_COLS = (CTAS_PER_SM == 2) ? 256 : 512;
     static constexpr uint32_t COL_O = 2 * BN;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(COL_O + D <= TMEM_COLS, "TMEM budget");
-    // one CTA per SM: two would not fit in the SM's shared memory, so a CTA
-    // never waits on another's 512 TMEM columns
-    static_assert(2 * SMEM_ALLOC > 233472, "one CTA per SM");
+    // at most CTAS_PER_SM CTAs fit in an SM's 228 KB (1 KB reserved per CTA),
+    // and together they never ask for more than the SM's 512 TMEM columns, so
+    // no tcgen05.alloc waits on another CTA
+    static_assert(CTAS_PER_SM * (SMEM_ALLOC + 1024) <= 233472, "CTAs per SM fit");
+    static_assert((CTAS_PER_SM + 1) * (SMEM_ALLOC + 1024) > 233472, "no extra CTA per SM");
+    static_assert(CTAS_PER_SM * TMEM_COLS <= 512, "TMEM per SM");
 };
 
 struct PrefillArgs {
@@ -74,7 +80,7 @@ struct PrefillArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, PrefillCfg<D>::CTAS_PER_SM)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
     using C = PrefillCfg<D>;
@@ -324,9 +330,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         const int i = c * 64 + u * 8 + e * 2;
                         const float x0 = raw ? fmaf(t[i], scale_log2, -m_off) : t[i] - m_off;
                         const float x1 = raw ? fmaf(t[i + 1], scale_log2, -m_off) : t[i + 1] - m_off;
-                        const __half2 hp = __floats2half2_rn(ex2_approx(x0), ex2_approx(x1));
-                        const float2 back = __half22float2(hp);
-                        lsum += back.x + back.y;
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        const __half2 hp = __floats2half2_rn(p0, p1);
+                        lsum += p0 + p1;
                         packed[e] = *reinterpret_cast<const uint32_t*>(&hp);
                     }
                     const int sw = (u ^ (row & 7)) * 16;
