@@ -10,9 +10,11 @@
 // with 1-16 queries per workgroup; here a CTA owns a 128-query tile and the
 // two contractions run on tcgen05:
 //
-//   S_j  = Q K_j^T     128 x BN, f32 in TMEM        (tcgen05.mma, A,B in smem)
-//   P_j  = exp2(S_j * scale*log2e - m)  f16 -> smem (4 softmax warps, 1 row/thread)
-//   O   += P_j V_j     128 x D,  f32 in TMEM        (tcgen05.mma, V MN-major)
+//   S_j  = Q K_j^T     128 x BN, f32 in TMEM    (tcgen05.mma, Q and K in smem)
+//   P_j  = exp2(S_j * scale*log2e - m)         (4 softmax warps, 1 row/thread),
+//                      f16 written back to TMEM with tcgen05.st
+//   O   += P_j V_j     128 x D,  f32 in TMEM    (tcgen05.mma, P from TMEM,
+//                                               V in smem as the MN-major operand)
 //
 // Roles (192 threads): warps 0-3 softmax + epilogue (thread t owns query row t
 // = TMEM lane t), warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer.
@@ -35,6 +37,10 @@ constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
+// Softmax modes (compile-time): positive scale without a cap works on raw
+// accumulators; otherwise logits are scaled (and capped) first.
+enum : int { kModeRaw = 0, kModeScaled = 1, kModeCapped = 2 };
+
 template <int D>
 struct PrefillCfg {
     static constexpr int NCH = D / 64;                   // 64-element (128-byte) chunks of D
@@ -42,26 +48,26 @@ struct PrefillCfg {
     // two softmax warpgroups share every SM; D=128/256 run one CTA per SM.
     static constexpr int CTAS_PER_SM = (D == 64) ? 2 : 1;
     static constexpr int BN = (D == 128) ? 128 : 64;     // keys per tile
-    static constexpr int STAGES = (D == 64) ? 3 : 2;     // K/V ring depth
-    static constexpr int PCH = BN / 64;                  // 64-key chunks of a P row
+    static constexpr int STAGES = (D == 64) ? 5 : 2;     // K/V ring depth
     static constexpr uint32_t Q_BYTES = NCH * BM * 128;
     static constexpr uint32_t KV_CHUNK = BN * 128;       // one 64-column box of a K or V tile
     static constexpr uint32_t KV_BYTES = NCH * KV_CHUNK; // one K (or V) tile
-    static constexpr uint32_t P_BYTES = PCH * BM * 128;
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-    static constexpr uint32_t OFF_P = OFF_V + STAGES * KV_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
     // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2], teardown
     static constexpr int N_BARS = 1 + 3 * STAGES + 6 + 1;
     static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // slack for 1024-byte alignment
-    static constexpr uint32_t TMEM_COLS = (CTAS_PER_SM == 2) ? 256 : 512;
+    // TMEM columns: S double buffer, O, P double buffer (f16 pairs per column)
     static constexpr uint32_t COL_O = 2 * BN;
+    static constexpr uint32_t COL_P = COL_O + D;
+    static constexpr uint32_t P_COLS = BN / 2;
+    static constexpr uint32_t TMEM_COLS = (CTAS_PER_SM == 2) ? 256 : 512;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-    static_assert(COL_O + D <= TMEM_COLS, "TMEM budget");
+    static_assert(COL_P + 2 * P_COLS <= TMEM_COLS, "TMEM budget");
     // at most CTAS_PER_SM CTAs fit in an SM's 228 KB (1 KB reserved per CTA),
     // and together they never ask for more than the SM's 512 TMEM columns, so
     // no tcgen05.alloc waits on another CTA
@@ -70,16 +76,73 @@ struct PrefillCfg {
     static_assert(CTAS_PER_SM * TMEM_COLS <= 512, "TMEM per SM");
 };
 
+// Elements of every 8 in a P row whose exponential runs on the FMA pipe
+// (ex2_poly) instead of the MUFU unit; the rest use ex2.approx.
+constexpr int kPolyPerEight = 2;
+
+// 2^x on the FMA/ALU pipes: n = round(x) (added to the float 1.5*2^23 so that
+// the rounding lands n in the low mantissa bits), f = x - n in [-1/2, 1/2],
+// 2^f by a cubic minimax fit (relative error 7.5e-5, below the f16 rounding
+// of P; coefficients from fit_exp2_poly.py), then n is added to the exponent
+// field.  x is clamped at -125 so the exponent never underflows; such values
+// round to 0 in f16.
+__device__ __forceinline__ float ex2_poly(float x) {
+    x = fmaxf(x, -125.0f);
+    const float y = x + 12582912.0f;
+    const float n = y - 12582912.0f;
+    const float f = x - n;
+    const float p = fmaf(fmaf(fmaf(5.517166906e-02f, f, 2.426111222e-01f), f, 6.932609855e-01f), f,
+                         9.999280735e-01f);
+    return __uint_as_float(__float_as_uint(p) + (__float_as_uint(y) << 23));
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Max of a row of N logits with eight independent partial maxima (short
+// dependency chains) and three-input max instructions.
+template <int N>
+__device__ __forceinline__ float row_max(const float (&t)[N]) {
+    static_assert(N % 8 == 0 && N >= 16, "row length");
+    float a[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = t[k];
+    int i = 8;
+#pragma unroll
+    for (; i + 16 <= N; i += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) a[k] = max3(a[k], t[i + k], t[i + 8 + k]);
+#pragma unroll
+    for (; i < N; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) a[k] = fmaxf(a[k], t[i + k]);
+    return fmaxf(max3(a[0], a[1], a[2]), max3(a[3], a[4], fmaxf(a[5], max3(a[6], a[7], a[0]))));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A is read from TMEM (lane =
+// row, each 32-bit column holds two consecutive f16 elements of K).
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 struct PrefillArgs {
     __half* out;
     float* lse;
     int S, Hq, Hkv, causal, window;
     float softcap, scale;
-    int scale_positive;
     int* err;
 };
 
-template <int D>
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, PrefillCfg<D>::CTAS_PER_SM)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
@@ -215,13 +278,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const int st = j % STAGES;
                 if (!mbar_wait(bar(B_VFULL + st), (j / STAGES) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
                 tc_fence_after();
-                const uint32_t p_base = sbase + C::OFF_P + (j & 1) * C::P_BYTES;
+                const uint32_t p_tmem = tmem + C::COL_P + (j & 1) * C::P_COLS;
                 const uint32_t v_base = sbase + C::OFF_V + st * C::KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t a = smem_desc_sw128(p_base + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
+                    // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V (2048 bytes)
                     const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
-                    tc_mma_f16_ss(tmem + C::COL_O, a, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_f16_ts(tmem + C::COL_O, p_tmem + kk * 8, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(B_PVDONE + (j & 1)));
                 tc_commit(bar(B_KVEMPTY + st));
@@ -236,10 +299,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int row = threadIdx.x;           // 0..127 == TMEM lane
         const int qi = q0 + row;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const bool capped = args.softcap > 0.f;
         const float scale_log2 = args.scale * kLog2e;
         const float cap_log2 = args.softcap * kLog2e;
-        const float inv_cap_scale = capped ? args.scale / args.softcap : 0.f;
+        const float inv_cap_scale = MODE == kModeCapped ? args.scale / args.softcap : 0.f;
         float m_used = -INFINITY;   // running max actually used as the exponent offset (log2 units)
         float l_sum = 0.f;
         bool ok = true;
@@ -248,26 +310,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             float t[BN];
             {
-                uint32_t r[32];
+                uint32_t r[BN];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    tc_ld_32x32b_x32(lane_base + (j & 1) * BN + c * 32, r);
-                    tc_wait_ld();
+                for (int c = 0; c < BN / 32; ++c)
+                    tc_ld_32x32b_x32(lane_base + (j & 1) * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
+                tc_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) t[c * 32 + i] = __uint_as_float(r[i]);
-                }
+                for (int i = 0; i < BN; ++i) t[i] = __uint_as_float(r[i]);
             }
             const int key0 = (jt0 + j) * BN;
             const int key_last = key0 + BN - 1;
             bool full = key_last < S;
             if (args.causal) full = full && key_last <= qi;
             if (W > 0) full = full && (qi - key0 < W) && (args.causal || key_last - qi < W);
-            // scaled logits in log2 units
-            float mx = -INFINITY;
-            if (capped) {
+            // logits in log2 units (the raw mode keeps accumulators and scales in the exponent)
+            if constexpr (MODE == kModeCapped) {
 #pragma unroll
                 for (int i = 0; i < BN; ++i) t[i] = cap_log2 * tanh_abs_accurate(t[i] * inv_cap_scale);
-            } else if (!args.scale_positive) {
+            } else if constexpr (MODE == kModeScaled) {
 #pragma unroll
                 for (int i = 0; i < BN; ++i) t[i] *= scale_log2;
             }
@@ -285,11 +345,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (!keep) t[i] = -INFINITY;
                 }
             }
-#pragma unroll
-            for (int i = 0; i < BN; ++i) mx = fmaxf(mx, t[i]);
-            // raw-accumulator path: the max of raw logits scaled is the scaled max
-            const bool raw = !capped && args.scale_positive;
-            const float m_tile = raw ? mx * scale_log2 : mx;
+            const float mx = row_max(t);
+            const float m_tile = MODE == kModeRaw ? mx * scale_log2 : mx;
             const bool need = m_tile > m_used + kRescaleThreshold || (m_used == -INFINITY && m_tile > -INFINITY);
             if (__any_sync(0xffffffffu, need)) {
                 const float m_new = need ? fmaxf(m_tile, m_used) : m_used;
@@ -318,30 +375,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
             // P buffer (j & 1) is free once PV_{j-2} has retired
             if (j >= 2 && !mbar_wait(bar(B_PVDONE + (j & 1)), ((j - 2) >> 1) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
-            uint8_t* prow = smem + C::OFF_P + (j & 1) * C::P_BYTES + row * 128;
-            float lsum = 0.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};   // independent partial sums (short dependency chains)
+            uint32_t packed[BN / 2];
 #pragma unroll
-            for (int c = 0; c < C::PCH; ++c) {
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    uint32_t packed[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = c * 64 + u * 8 + e * 2;
-                        const float x0 = raw ? fmaf(t[i], scale_log2, -m_off) : t[i] - m_off;
-                        const float x1 = raw ? fmaf(t[i + 1], scale_log2, -m_off) : t[i + 1] - m_off;
-                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        const __half2 hp = __floats2half2_rn(p0, p1);
-                        lsum += p0 + p1;
-                        packed[e] = *reinterpret_cast<const uint32_t*>(&hp);
-                    }
-                    const int sw = (u ^ (row & 7)) * 16;
-                    *reinterpret_cast<uint4*>(prow + c * (BM * 128) + sw) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                }
+            for (int i = 0; i < BN; i += 2) {
+                const int e = (i / 2) & 3;
+                const float x0 = MODE == kModeRaw ? fmaf(t[i], scale_log2, -m_off) : t[i] - m_off;
+                const float x1 = MODE == kModeRaw ? fmaf(t[i + 1], scale_log2, -m_off) : t[i + 1] - m_off;
+                const bool poly = (i & 7) < kPolyPerEight;
+                const float p0 = poly ? ex2_poly(x0) : ex2_approx(x0);
+                const float p1 = poly ? ex2_poly(x1) : ex2_approx(x1);
+                const __half2 hp = __floats2half2_rn(p0, p1);
+                ls[e] += p0 + p1;
+                packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
             }
-            l_sum += lsum;
-            fence_proxy_async_smem();
+            l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            const uint32_t p_addr = lane_base + C::COL_P + (j & 1) * C::P_COLS;
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+                tc_st_32x32b_x32(p_addr + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(packed + c * 32));
+            tc_wait_st();
             tc_fence_before();
             mbar_arrive(bar(B_PFULL + (j & 1)));
         }
@@ -386,8 +439,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
-template <int D>
-attn_status launch_prefill_d(const PrefillLaunch& L) {
+template <int D, int MODE>
+attn_status launch_prefill_dm(const PrefillLaunch& L) {
     using C = PrefillCfg<D>;
     CUtensorMap tq, tk, tv;
     attn_status st;
@@ -399,7 +452,7 @@ attn_status launch_prefill_d(const PrefillLaunch& L) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_tc_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_ALLOC) != cudaSuccess)
             return set_error(ATTN_ECUDA, "cudaFuncSetAttribute(prefill smem) failed");
         attr_set[dev] = true;
@@ -414,13 +467,19 @@ attn_status launch_prefill_d(const PrefillLaunch& L) {
     a.window = L.window;
     a.softcap = L.softcap;
     a.scale = L.scale;
-    a.scale_positive = L.scale > 0.f;
     a.err = L.err_word;
     dim3 grid((L.S + BM - 1) / BM, L.Hq);
-    prefill_tc_kernel<D><<<grid, kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
+    prefill_tc_kernel<D, MODE><<<grid, kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
+}
+
+template <int D>
+attn_status launch_prefill_d(const PrefillLaunch& L) {
+    if (L.softcap > 0.f) return launch_prefill_dm<D, kModeCapped>(L);
+    if (L.scale > 0.f) return launch_prefill_dm<D, kModeRaw>(L);
+    return launch_prefill_dm<D, kModeScaled>(L);
 }
 
 }  // namespace
