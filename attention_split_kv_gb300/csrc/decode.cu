@@ -175,28 +175,6 @@ __device__ void build_prefix(const DecArgs& A, int* pref, int* scratch) {
     __syncthreads();
 }
 
-// ---- packed fp32 helpers (sm_100 family f32x2 instructions)
-__device__ __forceinline__ uint64_t pk(float2 a) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
-    return r;
-}
-__device__ __forceinline__ float2 upk(uint64_t r) {
-    float2 a;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
-    return a;
-}
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
-    return upk(d);
-}
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
-    return upk(d);
-}
-
 // One lane's slice of a K or V row -> E floats (as E/2 pairs).
 template <int D, bool I8, int GH>
 __device__ __forceinline__ void load_row_slice(const uint8_t* row, int c, float2 (&x)[DecCfg<D, I8, GH>::E / 2]) {

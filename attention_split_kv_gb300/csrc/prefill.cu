@@ -77,8 +77,10 @@ struct PrefillCfg {
 };
 
 // Elements of every 8 in a P row whose exponential runs on the FMA pipe
-// (ex2_poly) instead of the MUFU unit; the rest use ex2.approx.
-constexpr int kPolyPerEight = 2;
+// (ex2_poly) instead of the MUFU unit; the rest use ex2.approx.  Measured on
+// GB300 with the current softmax (issue-bound rather than MUFU-bound): 0 of 8
+// is fastest for D=64 (579 vs 549 TFLOP/s at 2 of 8, 522 at 4 of 8).
+constexpr int kPolyPerEight = 0;
 
 // 2^x on the FMA/ALU pipes: n = round(x) (added to the float 1.5*2^23 so that
 // the rounding lands n in the low mantissa bits), f = x - n in [-1/2, 1/2],
@@ -94,6 +96,21 @@ __device__ __forceinline__ float ex2_poly(float x) {
     const float p = fmaf(fmaf(fmaf(5.517166906e-02f, f, 2.426111222e-01f), f, 6.932609855e-01f), f,
                          9.999280735e-01f);
     return __uint_as_float(__float_as_uint(p) + (__float_as_uint(y) << 23));
+}
+
+// Two elements of ex2_poly in packed f32x2 arithmetic.
+__device__ __forceinline__ float2 ex2_poly2(float2 x) {
+    x = make_float2(fmaxf(x.x, -125.0f), fmaxf(x.y, -125.0f));
+    const float2 magic = make_float2(12582912.0f, 12582912.0f);
+    const float2 y = fadd2(x, magic);
+    const float2 n = fadd2(y, make_float2(-12582912.0f, -12582912.0f));
+    const float2 f = fadd2(x, make_float2(-n.x, -n.y));
+    float2 p = ffma2(make_float2(5.517166906e-02f, 5.517166906e-02f), f,
+                     make_float2(2.426111222e-01f, 2.426111222e-01f));
+    p = ffma2(p, f, make_float2(6.932609855e-01f, 6.932609855e-01f));
+    p = ffma2(p, f, make_float2(9.999280735e-01f, 9.999280735e-01f));
+    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(y.x) << 23)),
+                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(y.y) << 23)));
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -375,21 +392,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
             // P buffer (j & 1) is free once PV_{j-2} has retired
             if (j >= 2 && !mbar_wait(bar(B_PVDONE + (j & 1)), ((j - 2) >> 1) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};   // independent partial sums (short dependency chains)
+            // pairs of elements in packed f32x2 arithmetic: x = t*scale - m (or t - m), p = 2^x
+            float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};   // independent partial sums (short dependency chains)
+            const float2 sl2 = make_float2(scale_log2, scale_log2);
+            const float2 nm2 = make_float2(-m_off, -m_off);
             uint32_t packed[BN / 2];
 #pragma unroll
             for (int i = 0; i < BN; i += 2) {
-                const int e = (i / 2) & 3;
-                const float x0 = MODE == kModeRaw ? fmaf(t[i], scale_log2, -m_off) : t[i] - m_off;
-                const float x1 = MODE == kModeRaw ? fmaf(t[i + 1], scale_log2, -m_off) : t[i + 1] - m_off;
+                const float2 ti = make_float2(t[i], t[i + 1]);
+                const float2 x = MODE == kModeRaw ? ffma2(ti, sl2, nm2) : fadd2(ti, nm2);
                 const bool poly = (i & 7) < kPolyPerEight;
-                const float p0 = poly ? ex2_poly(x0) : ex2_approx(x0);
-                const float p1 = poly ? ex2_poly(x1) : ex2_approx(x1);
-                const __half2 hp = __floats2half2_rn(p0, p1);
-                ls[e] += p0 + p1;
+                const float2 p = poly ? ex2_poly2(x) : make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                const __half2 hp = __floats2half2_rn(p.x, p.y);
+                ls[(i / 2) & 3] = fadd2(ls[(i / 2) & 3], p);
                 packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
             }
-            l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            const float2 lsum2 = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
+            l_sum += lsum2.x + lsum2.y;
             const uint32_t p_addr = lane_base + C::COL_P + (j & 1) * C::P_COLS;
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
