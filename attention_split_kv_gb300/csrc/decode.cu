@@ -358,6 +358,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const int hg = active ? u - g * A.HG : 0;
         const int hl = g - (I.hb * NW) / A.HG;   // this unit's kv head inside the tile
         float2 q2[GH][E / 2];
+        // int8 caches: q in 16-bit fixed point with one scale per head, so the
+        // dot with the raw int8 codes is exact integer arithmetic (dp2a); the
+        // only approximation is q's rounding to 1/32767 of its largest value
+        uint32_t qi[GH][E / 2];
+        float inv_qs[GH];
         if (active) {
 #pragma unroll
             for (int s = 0; s < GH; ++s) {
@@ -371,6 +376,37 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(qrow + dim));
                         q2[s][(v * C::EV + e) / 2] = make_float2(f.x * A.qscale, f.y * A.qscale);
                     }
+            }
+            if constexpr (I8) {
+                // per-head max |q| over the D dims held by the key's lanes; the
+                // partner at xor distance d holds this slot's head in slot s ^ rb(d)
+                float mq[GH];
+#pragma unroll
+                for (int s = 0; s < GH; ++s) {
+                    mq[s] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < E / 2; ++j) mq[s] = fmaxf(mq[s], fmaxf(fabsf(q2[s][j].x), fabsf(q2[s][j].y)));
+                }
+#pragma unroll
+                for (int k = 0; k < C::LOG_LPK; ++k) {
+                    const int d = LPK >> (k + 1);
+                    const int rb = k < C::LOG_GH ? (GH >> (k + 1)) : 0;
+                    float other[GH];
+#pragma unroll
+                    for (int s = 0; s < GH; ++s) other[s] = __shfl_xor_sync(0xffffffffu, mq[s ^ rb], d);
+#pragma unroll
+                    for (int s = 0; s < GH; ++s) mq[s] = fmaxf(mq[s], other[s]);
+                }
+#pragma unroll
+                for (int s = 0; s < GH; ++s) {
+                    const float qs = mq[s] > 0.f ? 32767.0f / mq[s] : 0.f;
+                    inv_qs[s] = mq[s] > 0.f ? mq[s] / 32767.0f : 0.f;
+#pragma unroll
+                    for (int j = 0; j < E / 2; ++j) {
+                        const int lo = __float2int_rn(q2[s][j].x * qs), hi = __float2int_rn(q2[s][j].y * qs);
+                        qi[s][j] = (static_cast<uint32_t>(lo) & 0xFFFFu) | (static_cast<uint32_t>(hi) << 16);
+                    }
+                }
             }
         }
         float2 o2[GH][E / 2];
@@ -400,29 +436,69 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
                 for (int st = 0; st < C::NSTEP; ++st) {
                     const int key = st * C::KPS + kk;
-                    float2 kx[E / 2];
-                    load_row_slice<D, I8, GH>(kt + (key * A.nh_box + hl) * C::RB, c, kx);
-                    float acc[GH];
+                    float t;
+                    if constexpr (I8) {
+                        // exact int32 dots of the int8 codes with the fixed-point q (dp2a)
+                        const uint8_t* krow = kt + (key * A.nh_box + hl) * C::RB;
+                        int acc[GH];
 #pragma unroll
-                    for (int s = 0; s < GH; ++s) {
-                        float2 a = make_float2(0.f, 0.f);
+                        for (int s = 0; s < GH; ++s) acc[s] = 0;
 #pragma unroll
-                        for (int j = 0; j < E / 2; ++j) a = ffma2(q2[s][j], kx[j], a);
-                        acc[s] = a.x + a.y;
+                        for (int v = 0; v < C::NV; ++v) {
+                            uint32_t w[C::VB / 4];
+                            if constexpr (C::VB == 16) {
+                                const uint4 x = *reinterpret_cast<const uint4*>(krow + (v * LPK + c) * C::VB);
+                                w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+                            } else {
+                                const uint2 x = *reinterpret_cast<const uint2*>(krow + (v * LPK + c) * C::VB);
+                                w[0] = x.x; w[1] = x.y;
+                            }
+#pragma unroll
+                            for (int i = 0; i < C::VB / 4; ++i)
+#pragma unroll
+                                for (int s = 0; s < GH; ++s) {
+                                    const int j = (v * C::EV) / 2 + 2 * i;
+                                    asm("dp2a.lo.s32.s32 %0, %1, %2, %0;" : "+r"(acc[s]) : "r"(qi[s][j]), "r"(w[i]));
+                                    asm("dp2a.hi.s32.s32 %0, %1, %2, %0;" : "+r"(acc[s]) : "r"(qi[s][j + 1]), "r"(w[i]));
+                                }
+                        }
+                        // reduce-scatter: after it, slot 0 holds the full dot of head `rot`
+#pragma unroll
+                        for (int k = 0; k < C::LOG_GH; ++k) {
+                            const int half = GH >> (k + 1);
+                            const int dist = LPK >> (k + 1);
+#pragma unroll
+                            for (int s = 0; s < half; ++s) acc[s] += __shfl_xor_sync(0xffffffffu, acc[s + half], dist);
+                        }
+#pragma unroll
+                        for (int dist = LPK >> (C::LOG_GH + 1); dist >= 1; dist >>= 1)
+                            acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], dist);
+                        t = static_cast<float>(acc[0]) * inv_qs[0] *
+                            __half2float(kst[(key / A.R) * (sbb / 2) + sc_off + (key % A.R)]);
+                    } else {
+                        float2 kx[E / 2];
+                        load_row_slice<D, I8, GH>(kt + (key * A.nh_box + hl) * C::RB, c, kx);
+                        float acc[GH];
+#pragma unroll
+                        for (int s = 0; s < GH; ++s) {
+                            float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int j = 0; j < E / 2; ++j) a = ffma2(q2[s][j], kx[j], a);
+                            acc[s] = a.x + a.y;
+                        }
+                        // reduce-scatter: after it, slot 0 holds the full dot of head `rot`
+#pragma unroll
+                        for (int k = 0; k < C::LOG_GH; ++k) {
+                            const int half = GH >> (k + 1);
+                            const int dist = LPK >> (k + 1);
+#pragma unroll
+                            for (int s = 0; s < half; ++s) acc[s] += __shfl_xor_sync(0xffffffffu, acc[s + half], dist);
+                        }
+#pragma unroll
+                        for (int dist = LPK >> (C::LOG_GH + 1); dist >= 1; dist >>= 1)
+                            acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], dist);
+                        t = acc[0];
                     }
-                    // reduce-scatter: after it, slot 0 holds the full dot of head `rot`
-#pragma unroll
-                    for (int k = 0; k < C::LOG_GH; ++k) {
-                        const int half = GH >> (k + 1);
-                        const int dist = LPK >> (k + 1);
-#pragma unroll
-                        for (int s = 0; s < half; ++s) acc[s] += __shfl_xor_sync(0xffffffffu, acc[s + half], dist);
-                    }
-#pragma unroll
-                    for (int dist = LPK >> (C::LOG_GH + 1); dist >= 1; dist >>= 1)
-                        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], dist);
-                    float t = acc[0];
-                    if (I8) t *= __half2float(kst[(key / A.R) * (sbb / 2) + sc_off + (key % A.R)]);
                     if (A.cap_log2 > 0.f) t = A.cap_log2 * tanh_abs_accurate(t);
                     tsc[st] = (key >= v_lo && key < v_hi) ? t : -INFINITY;
                 }
