@@ -41,6 +41,16 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 HEADLINE = "vision_2304"
+# DRAM bytes (read + write) per launch of each workload's kernels, from the ncu
+# captures summarised in profiles/ (decode captures were taken on reduced cases
+# and scaled by the tokens processed; traffic grows in proportion).  Set to
+# None whenever the kernel changes after the capture.
+NCU_TRAFFIC = {
+    "vision_2304": 14.21e6,
+    "swa_softcap_prefill": 33.63e6,
+    "paged_gqa_decode": 590.3e6,
+    "int8_long_decode": (136.5e6 + 8.3e6) * 8,
+}
 METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
 WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode"]
 L2_FLUSH_BYTES = 256 << 20
@@ -248,7 +258,7 @@ def run_reference(args, rank, world):
         total_t += dt
         flops += per_row * rows
     value = flops / total_t / 1e12
-    line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": 0,
+    line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) f16 inputs)",
@@ -386,7 +396,7 @@ def main(argv=None):
             peak = peaks["bf16_tflops"]
         results[n] = {"value": value, "unit": unit, "ms": t_ms, "launches_per_call": launches,
                       "roofline": {"bound": bound, "achieved": per_gpu, "peak": peak,
-                                   "unit": unit, "frac": per_gpu / peak, "traffic": None,
+                                   "unit": unit, "frac": per_gpu / peak, "traffic": NCU_TRAFFIC.get(n),
                                    "peak_source": peaks["source"],
                                    "scope": "whole call" if launches > 1 else "single kernel"}}
     if rank != 0:
