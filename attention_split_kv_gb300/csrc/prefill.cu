@@ -56,8 +56,10 @@ struct PrefillCfg {
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
-    // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2], teardown
-    static constexpr int N_BARS = 1 + 3 * STAGES + 6 + 1;
+    // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], pv_done[2],
+    // teardown.  K stages are released after their QK^T MMA and V stages after
+    // their PV MMA, so the next K tiles load while the softmax still runs.
+    static constexpr int N_BARS = 1 + 4 * STAGES + 6 + 1;
     static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // slack for 1024-byte alignment
@@ -174,8 +176,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int B_QFULL = 0;
-    const int B_KFULL = 1, B_VFULL = 1 + STAGES, B_KVEMPTY = 1 + 2 * STAGES;
-    const int B_SFULL = 1 + 3 * STAGES, B_PFULL = B_SFULL + 2, B_PVDONE = B_SFULL + 4;
+    const int B_KFULL = 1, B_VFULL = 1 + STAGES, B_KEMPTY = 1 + 2 * STAGES, B_VEMPTY = 1 + 3 * STAGES;
+    const int B_SFULL = 1 + 4 * STAGES, B_PFULL = B_SFULL + 2, B_PVDONE = B_SFULL + 4;
     const int B_TEARDOWN = B_SFULL + 6;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -199,7 +201,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(B_KFULL + s), 1);
             mbar_init(bar(B_VFULL + s), 1);
-            mbar_init(bar(B_KVEMPTY + s), 1);
+            mbar_init(bar(B_KEMPTY + s), 1);
+            mbar_init(bar(B_VEMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_SFULL + b), 1);
@@ -221,39 +224,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     if (warp == 4) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(bar(B_QFULL), C::Q_BYTES);
-            for (int c = 0; c < NCH; ++c)
-                tma_load_3d(sbase + C::OFF_Q + c * (BM * 128), &tm_q, bar(B_QFULL), c * 64, h, q0);
+        // lane 0 loads Q and the K tiles, lane 1 the V tiles; each waits only for
+        // its own stages to be released
+        if (lane == 0 || lane == 1) {
+            const bool is_k = lane == 0;
+            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+            const uint32_t off = is_k ? C::OFF_K : C::OFF_V;
+            const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
+            tma_prefetch_desc(tm);
+            if (is_k) {
+                tma_prefetch_desc(&tm_q);
+                mbar_arrive_expect_tx(bar(B_QFULL), C::Q_BYTES);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(sbase + C::OFF_Q + c * (BM * 128), &tm_q, bar(B_QFULL), c * 64, h, q0);
+            }
             int issued = 0;
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % STAGES;
                 if (j >= STAGES &&
-                    !mbar_wait(bar(B_KVEMPTY + st), ((j / STAGES) - 1) & 1, abort_flag, args.err, kErrTimeoutSlot))
+                    !mbar_wait(bar(b_empty + st), ((j / STAGES) - 1) & 1, abort_flag, args.err, kErrTimeoutSlot))
                     break;
                 const int key0 = (jt0 + j) * BN;
-                mbar_arrive_expect_tx(bar(B_KFULL + st), C::KV_BYTES);
+                mbar_arrive_expect_tx(bar(b_full + st), C::KV_BYTES);
                 for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(sbase + C::OFF_K + st * C::KV_BYTES + c * C::KV_CHUNK, &tm_k, bar(B_KFULL + st),
-                                c * 64, g, key0);
-                mbar_arrive_expect_tx(bar(B_VFULL + st), C::KV_BYTES);
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(sbase + C::OFF_V + st * C::KV_BYTES + c * C::KV_CHUNK, &tm_v, bar(B_VFULL + st),
-                                c * 64, g, key0);
+                    tma_load_3d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK, tm, bar(b_full + st), c * 64, g, key0);
                 issued = j + 1;
             }
             if (*abort_flag) {
                 // let copies already in flight land before the CTA's shared memory goes away
-                mbar_wait(bar(B_QFULL), 0, abort_flag, args.err, kErrTimeoutLoad);
-                for (int j = max(0, issued - STAGES); j < issued; ++j) {
-                    const int st = j % STAGES;
-                    volatile int never = 0;
-                    mbar_wait(bar(B_KFULL + st), (j / STAGES) & 1, &never, args.err, kErrTimeoutLoad);
-                    mbar_wait(bar(B_VFULL + st), (j / STAGES) & 1, &never, args.err, kErrTimeoutLoad);
-                }
+                volatile int never = 0;
+                if (is_k) mbar_wait(bar(B_QFULL), 0, &never, args.err, kErrTimeoutLoad);
+                for (int j = max(0, issued - STAGES); j < issued; ++j)
+                    mbar_wait(bar(b_full + (j % STAGES)), (j / STAGES) & 1, &never, args.err, kErrTimeoutLoad);
             }
         }
     } else if (warp == 5) {
@@ -276,6 +278,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     }
                 }
                 tc_commit(bar(B_SFULL + (j & 1)));
+                tc_commit(bar(B_KEMPTY + st));
             };
             if (ok && n_tiles > 0) {
                 ok = mbar_wait(bar(B_KFULL + 0), 0, abort_flag, args.err, kErrTimeoutLoad);
@@ -304,7 +307,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tc_mma_f16_ts(tmem + C::COL_O, p_tmem + kk * 8, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(B_PVDONE + (j & 1)));
-                tc_commit(bar(B_KVEMPTY + st));
+                tc_commit(bar(B_VEMPTY + st));
             }
             // all issued MMAs must retire before TMEM is released
             tc_commit(bar(B_TEARDOWN));
