@@ -48,14 +48,18 @@ struct PrefillCfg {
     // two softmax warpgroups share every SM; D=128/256 run one CTA per SM.
     static constexpr int CTAS_PER_SM = (D == 64) ? 2 : 1;
     static constexpr int BN = (D == 128) ? 128 : 64;     // keys per tile
-    static constexpr int STAGES = (D == 64) ? 5 : 2;     // K/V ring depth
+    // K/V ring depths: K is consumed a whole softmax earlier than V, so it gets
+    // the deeper ring where shared memory allows
+    static constexpr int KST = (D == 64) ? 5 : 3;
+    static constexpr int VST = (D == 64) ? 5 : 2;
+    static constexpr int STAGES = KST > VST ? KST : VST;  // barrier array size
     static constexpr uint32_t Q_BYTES = NCH * BM * 128;
     static constexpr uint32_t KV_CHUNK = BN * 128;       // one 64-column box of a K or V tile
     static constexpr uint32_t KV_BYTES = NCH * KV_CHUNK; // one K (or V) tile
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + KST * KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + VST * KV_BYTES;
     // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], pv_done[2],
     // teardown.  K stages are released after their QK^T MMA and V stages after
     // their PV MMA, so the next K tiles load while the softmax still runs.
@@ -231,6 +235,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
             const uint32_t off = is_k ? C::OFF_K : C::OFF_V;
             const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
+            const int NST = is_k ? C::KST : C::VST;
             tma_prefetch_desc(tm);
             if (is_k) {
                 tma_prefetch_desc(&tm_q);
@@ -240,9 +245,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             int issued = 0;
             for (int j = 0; j < n_tiles; ++j) {
-                const int st = j % STAGES;
-                if (j >= STAGES &&
-                    !mbar_wait(bar(b_empty + st), ((j / STAGES) - 1) & 1, abort_flag, args.err, kErrTimeoutSlot))
+                const int st = j % NST;
+                if (j >= NST &&
+                    !mbar_wait(bar(b_empty + st), ((j / NST) - 1) & 1, abort_flag, args.err, kErrTimeoutSlot))
                     break;
                 const int key0 = (jt0 + j) * BN;
                 mbar_arrive_expect_tx(bar(b_full + st), C::KV_BYTES);
@@ -254,8 +259,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 // let copies already in flight land before the CTA's shared memory goes away
                 volatile int never = 0;
                 if (is_k) mbar_wait(bar(B_QFULL), 0, &never, args.err, kErrTimeoutLoad);
-                for (int j = max(0, issued - STAGES); j < issued; ++j)
-                    mbar_wait(bar(b_full + (j % STAGES)), (j / STAGES) & 1, &never, args.err, kErrTimeoutLoad);
+                for (int j = max(0, issued - NST); j < issued; ++j)
+                    mbar_wait(bar(b_full + (j % NST)), (j / NST) & 1, &never, args.err, kErrTimeoutLoad);
             }
         }
     } else if (warp == 5) {
@@ -265,7 +270,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             constexpr uint32_t idesc_o = idesc_f16_f32(BM, D, true);
             bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, args.err, kErrTimeoutLoad);
             auto issue_s = [&](int j) {
-                const int st = j % STAGES;
+                const int st = j % C::KST;
                 const uint32_t d_tmem = tmem + (j & 1) * BN;
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
@@ -289,14 +294,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles) {
-                    const int st1 = (j + 1) % STAGES;
-                    if (!mbar_wait(bar(B_KFULL + st1), ((j + 1) / STAGES) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
+                    const int st1 = (j + 1) % C::KST;
+                    if (!mbar_wait(bar(B_KFULL + st1), ((j + 1) / C::KST) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
                     tc_fence_after();
                     issue_s(j + 1);
                 }
                 if (!mbar_wait(bar(B_PFULL + (j & 1)), (j >> 1) & 1, abort_flag, args.err, kErrTimeoutSoftmax)) break;
-                const int st = j % STAGES;
-                if (!mbar_wait(bar(B_VFULL + st), (j / STAGES) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
+                const int st = j % C::VST;
+                if (!mbar_wait(bar(B_VFULL + st), (j / C::VST) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
                 tc_fence_after();
                 const uint32_t p_tmem = tmem + C::COL_P + (j & 1) * C::P_COLS;
                 const uint32_t v_base = sbase + C::OFF_V + st * C::KV_BYTES;
