@@ -48,7 +48,7 @@ def test_prefill_window(D, causal, window):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("softcap", [5.0, 50.0])
+@pytest.mark.parametrize("softcap", [1.0, 5.0, 50.0])
 def test_prefill_softcap(D, softcap):
     pc = si.make_prefill_case(333, 4, 2, D, seed=int(softcap) + D, causal=True, window=100,
                               softcap=softcap, scale=1.0 / 16.0)
