@@ -44,14 +44,18 @@ enum : int { kModeRaw = 0, kModeScaled = 1, kModeCapped = 2 };
 template <int D>
 struct PrefillCfg {
     static constexpr int NCH = D / 64;                   // 64-element (128-byte) chunks of D
-    // D=64 runs two CTAs per SM (64-key tiles, 256 TMEM columns each) so that
-    // two softmax warpgroups share every SM; D=128/256 run one CTA per SM.
+    // D=64 runs two CTAs per SM (256 TMEM columns each) so that two softmax
+    // warpgroups share every SM; D=128/256 run one CTA per SM.
     static constexpr int CTAS_PER_SM = (D == 64) ? 2 : 1;
-    static constexpr int BN = (D == 128) ? 128 : 64;     // keys per tile
+    static constexpr int BN = (D == 256) ? 64 : 128;     // keys per tile
+    // S and P buffers in TMEM.  D=64 (two CTAs per SM, 256 columns each) keeps
+    // one of each: the softmax frees S as soon as its row is in registers, so
+    // the next QK^T still overlaps the exponentials.
+    static constexpr int NBUF = (D == 64) ? 1 : 2;
     // K/V ring depths: K is consumed a whole softmax earlier than V, so it gets
     // the deeper ring where shared memory allows
-    static constexpr int KST = (D == 64) ? 5 : 3;
-    static constexpr int VST = (D == 64) ? 5 : 2;
+    static constexpr int KST = 3;
+    static constexpr int VST = 2;
     static constexpr int STAGES = KST > VST ? KST : VST;  // barrier array size
     static constexpr uint32_t Q_BYTES = NCH * BM * 128;
     static constexpr uint32_t KV_CHUNK = BN * 128;       // one 64-column box of a K or V tile
@@ -61,19 +65,19 @@ struct PrefillCfg {
     static constexpr uint32_t OFF_V = OFF_K + KST * KV_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_V + VST * KV_BYTES;
     // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], pv_done[2],
-    // teardown.  K stages are released after their QK^T MMA and V stages after
+    // teardown, s_free.  K stages are released after their QK^T MMA and V stages after
     // their PV MMA, so the next K tiles load while the softmax still runs.
-    static constexpr int N_BARS = 1 + 4 * STAGES + 6 + 1;
+    static constexpr int N_BARS = 1 + 4 * STAGES + 6 + 1 + 1;
     static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // slack for 1024-byte alignment
-    // TMEM columns: S double buffer, O, P double buffer (f16 pairs per column)
-    static constexpr uint32_t COL_O = 2 * BN;
+    // TMEM columns: S buffers, O, P buffers (f16 pairs per column)
+    static constexpr uint32_t COL_O = NBUF * BN;
     static constexpr uint32_t COL_P = COL_O + D;
     static constexpr uint32_t P_COLS = BN / 2;
     static constexpr uint32_t TMEM_COLS = (CTAS_PER_SM == 2) ? 256 : 512;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-    static_assert(COL_P + 2 * P_COLS <= TMEM_COLS, "TMEM budget");
+    static_assert(COL_P + NBUF * P_COLS <= TMEM_COLS, "TMEM budget");
     // at most CTAS_PER_SM CTAs fit in an SM's 228 KB (1 KB reserved per CTA),
     // and together they never ask for more than the SM's 512 TMEM columns, so
     // no tcgen05.alloc waits on another CTA
@@ -183,6 +187,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int B_KFULL = 1, B_VFULL = 1 + STAGES, B_KEMPTY = 1 + 2 * STAGES, B_VEMPTY = 1 + 3 * STAGES;
     const int B_SFULL = 1 + 4 * STAGES, B_PFULL = B_SFULL + 2, B_PVDONE = B_SFULL + 4;
     const int B_TEARDOWN = B_SFULL + 6;
+    const int B_SFREE = B_SFULL + 7;     // softmax has S in registers (single S buffer only)
+    constexpr int NBUF = C::NBUF;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = args.S;
@@ -214,6 +220,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(bar(B_PVDONE + b), 1);
         }
         mbar_init(bar(B_TEARDOWN), 1);
+        mbar_init(bar(B_SFREE), 4 * 32);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -271,7 +278,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, args.err, kErrTimeoutLoad);
             auto issue_s = [&](int j) {
                 const int st = j % C::KST;
-                const uint32_t d_tmem = tmem + (j & 1) * BN;
+                const uint32_t d_tmem = tmem + (j % NBUF) * BN;
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
 #pragma unroll
@@ -282,7 +289,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         tc_mma_f16_ss(d_tmem, a, b, idesc_s, (c | kk) != 0);
                     }
                 }
-                tc_commit(bar(B_SFULL + (j & 1)));
+                tc_commit(bar(B_SFULL + (j % NBUF)));
                 tc_commit(bar(B_KEMPTY + st));
             };
             if (ok && n_tiles > 0) {
@@ -295,15 +302,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles) {
                     const int st1 = (j + 1) % C::KST;
+                    // a single S buffer is overwritten only once the softmax holds S_j in registers
+                    if (NBUF == 1 &&
+                        !mbar_wait(bar(B_SFREE), j & 1, abort_flag, args.err, kErrTimeoutSoftmax)) break;
                     if (!mbar_wait(bar(B_KFULL + st1), ((j + 1) / C::KST) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
                     tc_fence_after();
                     issue_s(j + 1);
                 }
-                if (!mbar_wait(bar(B_PFULL + (j & 1)), (j >> 1) & 1, abort_flag, args.err, kErrTimeoutSoftmax)) break;
+                if (!mbar_wait(bar(B_PFULL + (j % NBUF)), (j / NBUF) & 1, abort_flag, args.err, kErrTimeoutSoftmax)) break;
                 const int st = j % C::VST;
                 if (!mbar_wait(bar(B_VFULL + st), (j / C::VST) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
                 tc_fence_after();
-                const uint32_t p_tmem = tmem + C::COL_P + (j & 1) * C::P_COLS;
+                const uint32_t p_tmem = tmem + C::COL_P + (j % NBUF) * C::P_COLS;
                 const uint32_t v_base = sbase + C::OFF_V + st * C::KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
@@ -311,7 +321,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
                     tc_mma_f16_ts(tmem + C::COL_O, p_tmem + kk * 8, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(bar(B_PVDONE + (j & 1)));
+                tc_commit(bar(B_PVDONE + (j % NBUF)));
                 tc_commit(bar(B_VEMPTY + st));
             }
             // all issued MMAs must retire before TMEM is released
@@ -331,14 +341,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles && ok; ++j) {
-            if (!mbar_wait(bar(B_SFULL + (j & 1)), (j >> 1) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
+            if (!mbar_wait(bar(B_SFULL + (j % NBUF)), (j / NBUF) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
             tc_fence_after();
             float t[BN];
             {
                 uint32_t r[BN];
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c)
-                    tc_ld_32x32b_x32(lane_base + (j & 1) * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
+                    tc_ld_32x32b_x32(lane_base + (j % NBUF) * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
                 tc_wait_ld();
 #pragma unroll
                 for (int i = 0; i < BN; ++i) t[i] = __uint_as_float(r[i]);
@@ -374,7 +384,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     uint32_t r[BN];
 #pragma unroll
                     for (int c = 0; c < BN / 32; ++c)
-                        tc_ld_32x32b_x32(lane_base + (j & 1) * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
+                        tc_ld_32x32b_x32(lane_base + (j % NBUF) * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
                     tc_wait_ld();
 #pragma unroll
                     for (int i = 0; i < BN; ++i)
@@ -383,6 +393,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             } else if constexpr (MODE == kModeScaled) {
 #pragma unroll
                 for (int i = 0; i < BN; ++i) t[i] *= scale_log2;
+            }
+            if constexpr (NBUF == 1) {
+                // S_j is in registers: the MMA warp may write S_{j+1}
+                tc_fence_before();
+                mbar_arrive(bar(B_SFREE));
             }
             if (!full) {
 #pragma unroll
@@ -401,63 +416,66 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float mx = row_max(t);
             const float m_tile = MODE == kModeRaw ? mx * scale_log2 : mx;
             const bool need = m_tile > m_used + kRescaleThreshold || (m_used == -INFINITY && m_tile > -INFINITY);
-            if (__any_sync(0xffffffffu, need)) {
-                const float m_new = need ? fmaxf(m_tile, m_used) : m_used;
+            // the warp rescales O (below, once t[] is no longer live) if any of its rows moved its max
+            const bool rescale = __any_sync(0xffffffffu, need) && j > 0;
+            float alpha_o = 1.f;
+            if (need) {
+                const float m_new = fmaxf(m_tile, m_used);
                 const float alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
-                if (j > 0) {
-                    // O must not be in flight while it is rescaled
-                    if (!mbar_wait(bar(B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
-                    tc_fence_after();
-                    const float a = need ? alpha : 1.f;
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tc_ld_32x32b_x32(lane_base + C::COL_O + c * 32, r);
-                        tc_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
-                        tc_st_32x32b_x32(lane_base + C::COL_O + c * 32, r);
-                    }
-                    tc_wait_st();
-                }
-                if (need) {
-                    l_sum *= alpha;
-                    m_used = m_new;
-                }
+                alpha_o = alpha;
+                l_sum *= alpha;
+                m_used = m_new;
             }
             const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
-            // P buffer (j & 1) is free once PV_{j-2} has retired
-            if (j >= 2 && !mbar_wait(bar(B_PVDONE + (j & 1)), ((j - 2) >> 1) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
+            // P buffer j % NBUF is free once PV_{j-NBUF} has retired
+            if (j >= NBUF && !mbar_wait(bar(B_PVDONE + (j % NBUF)), ((j - NBUF) / NBUF) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
             // pairs of elements in packed f32x2 arithmetic: x = t*scale - m (or t - m), p = 2^x
             float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};   // independent partial sums (short dependency chains)
             const float2 sl2 = make_float2(scale_log2, scale_log2);
             const float2 nm2 = make_float2(-m_off, -m_off);
-            uint32_t packed[BN / 2];
+            const uint32_t p_addr = lane_base + C::COL_P + (j % NBUF) * C::P_COLS;
+            // 32 elements at a time, each chunk stored to TMEM as soon as it is packed
 #pragma unroll
-            for (int i = 0; i < BN; i += 2) {
-                const float2 ti = make_float2(t[i], t[i + 1]);
-                const float2 x = MODE == kModeRaw ? ffma2(ti, sl2, nm2) : fadd2(ti, nm2);
-                const bool poly = (i & 7) < kPolyPerEight;
-                const float2 p = poly ? ex2_poly2(x) : make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                const __half2 hp = __floats2half2_rn(p.x, p.y);
-                ls[(i / 2) & 3] = fadd2(ls[(i / 2) & 3], p);
-                packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float2 ti = make_float2(t[c * 32 + i], t[c * 32 + i + 1]);
+                    const float2 x = MODE == kModeRaw ? ffma2(ti, sl2, nm2) : fadd2(ti, nm2);
+                    const bool poly = (i & 7) < kPolyPerEight;
+                    const float2 p = poly ? ex2_poly2(x) : make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    const __half2 hp = __floats2half2_rn(p.x, p.y);
+                    ls[(i / 2) & 3] = fadd2(ls[(i / 2) & 3], p);
+                    packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+                }
+                tc_st_32x32b_x16(p_addr + c * 16, packed);
             }
             const float2 lsum2 = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
             l_sum += lsum2.x + lsum2.y;
-            const uint32_t p_addr = lane_base + C::COL_P + (j & 1) * C::P_COLS;
+            if (rescale) {
+                // O must not be in flight while it is rescaled (PV_j waits for p_full below)
+                if (NBUF > 1 &&
+                    !mbar_wait(bar(B_PVDONE + ((j - 1) % NBUF)), ((j - 1) / NBUF) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tc_ld_32x32b_x32(lane_base + C::COL_O + c * 32, r);
+                    tc_wait_ld();
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-                tc_st_32x32b_x32(p_addr + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(packed + c * 32));
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_o);
+                    tc_st_32x32b_x32(lane_base + C::COL_O + c * 32, r);
+                }
+            }
             tc_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL + (j & 1)));
+            mbar_arrive(bar(B_PFULL + (j % NBUF)));
         }
         // ------------------------------------------------------------ epilogue
         if (ok && n_tiles > 0) {
             const int jl = n_tiles - 1;
-            ok = mbar_wait(bar(B_PVDONE + (jl & 1)), (jl >> 1) & 1, abort_flag, args.err, kErrTimeoutMma);
+            ok = mbar_wait(bar(B_PVDONE + (jl % NBUF)), (jl / NBUF) & 1, abort_flag, args.err, kErrTimeoutMma);
         }
         if (ok) {
             tc_fence_after();
