@@ -33,7 +33,7 @@ def _check(pc, what=""):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("S", [1, 100, 128, 300, 515])
+@pytest.mark.parametrize("S", [1, 100, 128, 192, 300, 515])
 @pytest.mark.parametrize("causal", [True, False], ids=["causal", "bidir"])
 def test_prefill_plain(D, S, causal):
     pc = si.make_prefill_case(S, 2, 1, D, seed=S + D, causal=causal)
