@@ -16,8 +16,9 @@
 //   O   += P_j V_j     128 x D,  f32 in TMEM    (tcgen05.mma, P from TMEM,
 //                                               V in smem as the MN-major operand)
 //
-// Roles (192 threads): warps 0-3 softmax + epilogue (thread t owns query row t
-// = TMEM lane t), warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer.
+// Roles: warps 0-3 softmax + epilogue (thread t owns query row t = TMEM lane
+// t), warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer (D=64 adds two
+// idle warps 6-7 to complete the second warpgroup for setmaxnreg).
 // The MMA warp issues S_{j+1} before waiting for P_j, so QK^T of the next tile
 // overlaps the softmax of the current one.  O is rescaled lazily: only when a
 // row's running max grows by more than 8 (log2 units), so P <= 2^8 stays
@@ -33,7 +34,6 @@ namespace attn {
 namespace {
 
 constexpr int BM = 128;                 // queries per CTA (TMEM lanes)
-constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
@@ -47,6 +47,13 @@ struct PrefillCfg {
     // D=64 runs two CTAs per SM (256 TMEM columns each) so that two softmax
     // warpgroups share every SM; D=128/256 run one CTA per SM.
     static constexpr int CTAS_PER_SM = (D == 64) ? 2 : 1;
+    // D=64: two full warpgroups, so that setmaxnreg can move registers from
+    // the producer/MMA warpgroup (warps 4-7, two of them idle) to the softmax
+    // warpgroup: 2 CTAs x 256 threads x 128 registers at launch, then
+    // 128 x 200 + 128 x 56 per CTA.  D=128/256 (one CTA per SM) run 6 warps.
+    static constexpr int THREADS = (D == 64) ? 256 : 192;
+    static constexpr int REG_SOFTMAX = 200, REG_OTHER = 56;
+    static_assert(D != 64 || (REG_SOFTMAX + REG_OTHER) * 128 * CTAS_PER_SM == 65536, "register split");
     static constexpr int BN = (D == 256) ? 64 : 128;     // keys per tile
     // S and P buffers in TMEM.  D=64 (two CTAs per SM, 256 columns each) keeps
     // one of each: the softmax frees S as soon as its row is in registers, so
@@ -87,9 +94,10 @@ struct PrefillCfg {
 };
 
 // Elements of every 8 in a P row whose exponential runs on the FMA pipe
-// (ex2_poly) instead of the MUFU unit; the rest use ex2.approx.  Measured on
-// GB300 with the current softmax (issue-bound rather than MUFU-bound): 0 of 8
-// is fastest for D=64 (579 vs 549 TFLOP/s at 2 of 8, 522 at 4 of 8).
+// (ex2_poly2) instead of the MUFU unit; the rest use ex2.approx.  Measured on
+// GB300 (the MUFU unit is far from saturated here): 0 of 8 is fastest for D=64
+// (33.4 us per launch for S=2304, 16 heads, against 35.5 at 2 of 8, 37.5 at
+// 3 of 8 and 41.7 at 4 of 8).
 constexpr int kPolyPerEight = 0;
 
 // 2^x on the FMA/ALU pipes: n = round(x) (added to the float 1.5*2^23 so that
@@ -97,18 +105,7 @@ constexpr int kPolyPerEight = 0;
 // 2^f by a cubic minimax fit (relative error 7.5e-5, below the f16 rounding
 // of P; coefficients from fit_exp2_poly.py), then n is added to the exponent
 // field.  x is clamped at -125 so the exponent never underflows; such values
-// round to 0 in f16.
-__device__ __forceinline__ float ex2_poly(float x) {
-    x = fmaxf(x, -125.0f);
-    const float y = x + 12582912.0f;
-    const float n = y - 12582912.0f;
-    const float f = x - n;
-    const float p = fmaf(fmaf(fmaf(5.517166906e-02f, f, 2.426111222e-01f), f, 6.932609855e-01f), f,
-                         9.999280735e-01f);
-    return __uint_as_float(__float_as_uint(p) + (__float_as_uint(y) << 23));
-}
-
-// Two elements of ex2_poly in packed f32x2 arithmetic.
+// round to 0 in f16.  Two elements at a time, in packed f32x2 arithmetic.
 __device__ __forceinline__ float2 ex2_poly2(float2 x) {
     x = make_float2(fmaxf(x.x, -125.0f), fmaxf(x.y, -125.0f));
     const float2 magic = make_float2(12582912.0f, 12582912.0f);
@@ -121,6 +118,16 @@ __device__ __forceinline__ float2 ex2_poly2(float2 x) {
     p = ffma2(p, f, make_float2(9.999280735e-01f, 9.999280735e-01f));
     return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(y.x) << 23)),
                        __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(y.y) << 23)));
+}
+
+// Per-warpgroup register budgets (all four warps of a warpgroup execute these).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -170,7 +177,7 @@ struct PrefillArgs {
 };
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, PrefillCfg<D>::CTAS_PER_SM)
+__global__ void __launch_bounds__(PrefillCfg<D>::THREADS, PrefillCfg<D>::CTAS_PER_SM)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
     using C = PrefillCfg<D>;
@@ -233,104 +240,109 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ TMA producer
-        // lane 0 loads Q and the K tiles, lane 1 the V tiles; each waits only for
-        // its own stages to be released
-        if (lane == 0 || lane == 1) {
-            const bool is_k = lane == 0;
-            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
-            const uint32_t off = is_k ? C::OFF_K : C::OFF_V;
-            const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
-            const int NST = is_k ? C::KST : C::VST;
-            tma_prefetch_desc(tm);
-            if (is_k) {
-                tma_prefetch_desc(&tm_q);
-                mbar_arrive_expect_tx(bar(B_QFULL), C::Q_BYTES);
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(sbase + C::OFF_Q + c * (BM * 128), &tm_q, bar(B_QFULL), c * 64, h, q0);
+    if (warp >= 4) {
+        // (setmaxnreg is executed by all four warps of a warpgroup)
+        if constexpr (C::THREADS == 256) setmaxnreg_dec<C::REG_OTHER>();
+        if (warp == 4) {
+            // ------------------------------------------------------------ TMA producer
+            // lane 0 loads Q and the K tiles, lane 1 the V tiles; each waits only for
+            // its own stages to be released
+            if (lane == 0 || lane == 1) {
+                const bool is_k = lane == 0;
+                const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+                const uint32_t off = is_k ? C::OFF_K : C::OFF_V;
+                const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
+                const int NST = is_k ? C::KST : C::VST;
+                tma_prefetch_desc(tm);
+                if (is_k) {
+                    tma_prefetch_desc(&tm_q);
+                    mbar_arrive_expect_tx(bar(B_QFULL), C::Q_BYTES);
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_3d(sbase + C::OFF_Q + c * (BM * 128), &tm_q, bar(B_QFULL), c * 64, h, q0);
+                }
+                int issued = 0;
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int st = j % NST;
+                    if (j >= NST &&
+                        !mbar_wait(bar(b_empty + st), ((j / NST) - 1) & 1, abort_flag, args.err, kErrTimeoutSlot))
+                        break;
+                    const int key0 = (jt0 + j) * BN;
+                    mbar_arrive_expect_tx(bar(b_full + st), C::KV_BYTES);
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_3d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK, tm, bar(b_full + st), c * 64, g, key0);
+                    issued = j + 1;
+                }
+                if (*abort_flag) {
+                    // let copies already in flight land before the CTA's shared memory goes away
+                    volatile int never = 0;
+                    if (is_k) mbar_wait(bar(B_QFULL), 0, &never, args.err, kErrTimeoutLoad);
+                    for (int j = max(0, issued - NST); j < issued; ++j)
+                        mbar_wait(bar(b_full + (j % NST)), (j / NST) & 1, &never, args.err, kErrTimeoutLoad);
+                }
             }
-            int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j % NST;
-                if (j >= NST &&
-                    !mbar_wait(bar(b_empty + st), ((j / NST) - 1) & 1, abort_flag, args.err, kErrTimeoutSlot))
-                    break;
-                const int key0 = (jt0 + j) * BN;
-                mbar_arrive_expect_tx(bar(b_full + st), C::KV_BYTES);
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK, tm, bar(b_full + st), c * 64, g, key0);
-                issued = j + 1;
-            }
-            if (*abort_flag) {
-                // let copies already in flight land before the CTA's shared memory goes away
-                volatile int never = 0;
-                if (is_k) mbar_wait(bar(B_QFULL), 0, &never, args.err, kErrTimeoutLoad);
-                for (int j = max(0, issued - NST); j < issued; ++j)
-                    mbar_wait(bar(b_full + (j % NST)), (j / NST) & 1, &never, args.err, kErrTimeoutLoad);
-            }
-        }
-    } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16_f32(BM, BN, false);
-            constexpr uint32_t idesc_o = idesc_f16_f32(BM, D, true);
-            bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, args.err, kErrTimeoutLoad);
-            auto issue_s = [&](int j) {
-                const int st = j % C::KST;
-                const uint32_t d_tmem = tmem + (j % NBUF) * BN;
+        } else if (warp == 5) {
+            // ------------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idesc_s = idesc_f16_f32(BM, BN, false);
+                constexpr uint32_t idesc_o = idesc_f16_f32(BM, D, true);
+                bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, args.err, kErrTimeoutLoad);
+                auto issue_s = [&](int j) {
+                    const int st = j % C::KST;
+                    const uint32_t d_tmem = tmem + (j % NBUF) * BN;
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) {
+                    for (int c = 0; c < NCH; ++c) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = smem_desc_sw128(sbase + C::OFF_Q + c * (BM * 128) + kk * 32, 16, 1024);
-                        const uint64_t b = smem_desc_sw128(
-                            sbase + C::OFF_K + st * C::KV_BYTES + c * C::KV_CHUNK + kk * 32, 16, 1024);
-                        tc_mma_f16_ss(d_tmem, a, b, idesc_s, (c | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = smem_desc_sw128(sbase + C::OFF_Q + c * (BM * 128) + kk * 32, 16, 1024);
+                            const uint64_t b = smem_desc_sw128(
+                                sbase + C::OFF_K + st * C::KV_BYTES + c * C::KV_CHUNK + kk * 32, 16, 1024);
+                            tc_mma_f16_ss(d_tmem, a, b, idesc_s, (c | kk) != 0);
+                        }
+                    }
+                    tc_commit(bar(B_SFULL + (j % NBUF)));
+                    tc_commit(bar(B_KEMPTY + st));
+                };
+                if (ok && n_tiles > 0) {
+                    ok = mbar_wait(bar(B_KFULL + 0), 0, abort_flag, args.err, kErrTimeoutLoad);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_s(0);
                     }
                 }
-                tc_commit(bar(B_SFULL + (j % NBUF)));
-                tc_commit(bar(B_KEMPTY + st));
-            };
-            if (ok && n_tiles > 0) {
-                ok = mbar_wait(bar(B_KFULL + 0), 0, abort_flag, args.err, kErrTimeoutLoad);
-                if (ok) {
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    if (j + 1 < n_tiles) {
+                        const int st1 = (j + 1) % C::KST;
+                        // a single S buffer is overwritten only once the softmax holds S_j in registers
+                        if (NBUF == 1 &&
+                            !mbar_wait(bar(B_SFREE), j & 1, abort_flag, args.err, kErrTimeoutSoftmax)) break;
+                        if (!mbar_wait(bar(B_KFULL + st1), ((j + 1) / C::KST) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
+                        tc_fence_after();
+                        issue_s(j + 1);
+                    }
+                    if (!mbar_wait(bar(B_PFULL + (j % NBUF)), (j / NBUF) & 1, abort_flag, args.err, kErrTimeoutSoftmax)) break;
+                    const int st = j % C::VST;
+                    if (!mbar_wait(bar(B_VFULL + st), (j / C::VST) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
                     tc_fence_after();
-                    issue_s(0);
-                }
-            }
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles) {
-                    const int st1 = (j + 1) % C::KST;
-                    // a single S buffer is overwritten only once the softmax holds S_j in registers
-                    if (NBUF == 1 &&
-                        !mbar_wait(bar(B_SFREE), j & 1, abort_flag, args.err, kErrTimeoutSoftmax)) break;
-                    if (!mbar_wait(bar(B_KFULL + st1), ((j + 1) / C::KST) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
-                    tc_fence_after();
-                    issue_s(j + 1);
-                }
-                if (!mbar_wait(bar(B_PFULL + (j % NBUF)), (j / NBUF) & 1, abort_flag, args.err, kErrTimeoutSoftmax)) break;
-                const int st = j % C::VST;
-                if (!mbar_wait(bar(B_VFULL + st), (j / C::VST) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
-                tc_fence_after();
-                const uint32_t p_tmem = tmem + C::COL_P + (j % NBUF) * C::P_COLS;
-                const uint32_t v_base = sbase + C::OFF_V + st * C::KV_BYTES;
+                    const uint32_t p_tmem = tmem + C::COL_P + (j % NBUF) * C::P_COLS;
+                    const uint32_t v_base = sbase + C::OFF_V + st * C::KV_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V (2048 bytes)
-                    const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
-                    tc_mma_f16_ts(tmem + C::COL_O, p_tmem + kk * 8, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V (2048 bytes)
+                        const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
+                        tc_mma_f16_ts(tmem + C::COL_O, p_tmem + kk * 8, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(bar(B_PVDONE + (j % NBUF)));
+                    tc_commit(bar(B_VEMPTY + st));
                 }
-                tc_commit(bar(B_PVDONE + (j % NBUF)));
-                tc_commit(bar(B_VEMPTY + st));
+                // all issued MMAs must retire before TMEM is released
+                tc_commit(bar(B_TEARDOWN));
+                volatile int never = 0;
+                mbar_wait(bar(B_TEARDOWN), 0, &never, args.err, kErrTimeoutMma);
             }
-            // all issued MMAs must retire before TMEM is released
-            tc_commit(bar(B_TEARDOWN));
-            volatile int never = 0;
-            mbar_wait(bar(B_TEARDOWN), 0, &never, args.err, kErrTimeoutMma);
         }
     } else {
         // ------------------------------------------------------------ softmax warps
+        if constexpr (C::THREADS == 256) setmaxnreg_inc<C::REG_SOFTMAX>();
         const int row = threadIdx.x;           // 0..127 == TMEM lane
         const int qi = q0 + row;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
@@ -543,7 +555,7 @@ attn_status launch_prefill_dm(const PrefillLaunch& L) {
     a.scale = L.scale;
     a.err = L.err_word;
     dim3 grid((L.S + BM - 1) / BM, L.Hq);
-    prefill_tc_kernel<D, MODE><<<grid, kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
+    prefill_tc_kernel<D, MODE><<<grid, C::THREADS, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
