@@ -127,6 +127,24 @@ attn_status encode_tmap_plain(CUtensorMap* map, const void* base, CUtensorMapDat
     return ATTN_OK;
 }
 
+attn_status encode_tmap_sw128(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int rank,
+                              const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return set_error(ATTN_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t d[5], s[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    CUresult r = enc(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(ATTN_ECUDA, "cuTensorMapEncodeTiled (swizzled) failed (%d)", (int)r);
+    return ATTN_OK;
+}
+
 attn_status encode_tmap_3d_f16_sw128(CUtensorMap* map, const void* base, int D, int H, int S, int box_rows) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return set_error(ATTN_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");

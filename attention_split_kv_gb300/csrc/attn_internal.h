@@ -40,6 +40,9 @@ attn_status encode_tmap_3d_f16_sw128(CUtensorMap* map, const void* base, int D, 
 attn_status encode_tmap_plain(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int rank,
                               const uint64_t* dims, const uint64_t* strides_bytes,
                               const uint32_t* box);
+// Same, with the 128-byte swizzle (box rows of 128 bytes, as tcgen05 operands read them).
+attn_status encode_tmap_sw128(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int rank,
+                              const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
 
 // ---- prefill
 struct PrefillLaunch {

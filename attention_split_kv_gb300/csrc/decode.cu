@@ -597,6 +597,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     }
 }
 
+#include "decode_tc.cuh"
+
 // One warp per (sequence, query head): log-sum-exp merge of the splits.
 template <int D>
 __global__ void __launch_bounds__(128)
@@ -643,12 +645,117 @@ decode_combine_kernel(const int32_t* __restrict__ kv_len, const int32_t* __restr
         lse_out[(size_t)b * Hq + h] = wsum > 0.f ? (M + __log2f(wsum)) * 0.6931471805599453f : -INFINITY;
 }
 
+// Kernel arguments shared by both split kernels.
+DecArgs make_dec_args(const DecodeLaunch& L, const DecodePlan& plan, int R) {
+    const bool paged = L.page_table != nullptr;
+    const int cap_layout = paged ? L.max_pages * L.page_size : L.max_kv;
+    DecArgs a;
+    a.q = static_cast<const __half*>(L.q);
+    a.kv_len = L.kv_len;
+    a.page_table = L.page_table;
+    uint8_t* ws = static_cast<uint8_t*>(L.workspace);
+    a.ws_prefix = reinterpret_cast<int32_t*>(ws);
+    a.ws_lse = reinterpret_cast<float*>(ws + plan.off_lse);
+    a.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
+    a.B = L.B;
+    a.Hq = L.Hq;
+    a.Hkv = L.Hkv;
+    a.G = L.Hq / L.Hkv;
+    a.HG = plan.HG;
+    a.U = L.Hkv * plan.HG;
+    a.n_hb = plan.n_hb;
+    a.nh_box = plan.nh_box;
+    a.split = plan.split;
+    a.cap_eff = cap_layout < L.max_kv ? cap_layout : L.max_kv;
+    a.window = L.window;
+    a.P = paged ? L.page_size : 0;
+    a.R = R;
+    a.max_pages = L.max_pages;
+    a.n_pages = paged ? L.n_pages : 0;
+    a.paged = paged;
+    const bool capped = L.softcap > 0.f;
+    a.qscale = capped ? L.scale / L.softcap : L.scale * kLog2e;
+    a.cap_log2 = capped ? L.softcap * kLog2e : 0.f;
+    a.err = L.err_word;
+    return a;
+}
+
+template <int D>
+attn_status launch_combine(const DecodeLaunch& L, const DecodePlan& plan, const DecArgs& a) {
+    const int nwarps = L.B * L.Hq;
+    decode_combine_kernel<D><<<(nwarps + 3) / 4, 128, 0, L.stream>>>(
+        L.kv_len, a.ws_prefix, a.ws_lse, a.ws_o, static_cast<__half*>(L.out), L.lse, L.B, L.Hq, a.G, plan.GH,
+        plan.HG, plan.split, a.cap_eff, L.window);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode combine launch failed: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
+int decode_grid(const DecodePlan& plan) {
+    long grid = sm_count();
+    if (plan.max_items < grid) grid = plan.max_items;
+    return grid < 1 ? 1 : (int)grid;
+}
+
+// Tensor-core split kernel: f16 caches, head_dim 64/128, boxes of 16 rows x NH heads.
+template <int D, int NH>
+attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan) {
+    using C = tcdec::Cfg<D>;
+    const bool paged = L.page_table != nullptr;
+    CUtensorMap tk, tv;
+    attn_status st;
+    {
+        // [pages or B][rows][Hkv][D]: boxes of (64 dims, NH heads, 16 rows, 1), 128-byte swizzle
+        uint64_t dims[4], strides[3];
+        const uint32_t box[4] = {64u, (uint32_t)NH, 16u, 1u};
+        dims[0] = D;
+        dims[1] = L.Hkv;
+        dims[2] = paged ? L.page_size : L.max_kv;
+        dims[3] = paged ? L.n_pages : L.B;
+        strides[0] = (uint64_t)D * 2;
+        strides[1] = strides[0] * L.Hkv;
+        strides[2] = strides[1] * dims[2];
+        if ((st = encode_tmap_sw128(&tk, L.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, dims, strides, box)) != ATTN_OK)
+            return st;
+        if ((st = encode_tmap_sw128(&tv, L.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, dims, strides, box)) != ATTN_OK)
+            return st;
+    }
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(tcdec::decode_tc_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM_ALLOC) != cudaSuccess)
+            return set_error(ATTN_ECUDA, "cudaFuncSetAttribute(decode tc smem) failed");
+        attr_set[dev] = true;
+    }
+    const DecArgs a = make_dec_args(L, plan, 16);
+    tcdec::decode_tc_kernel<D, NH><<<decode_grid(plan), tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tk, tv, a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode tc launch failed: %s", cudaGetErrorString(e));
+    return launch_combine<D>(L, plan, a);
+}
+
 template <int D, bool I8, int GH>
 attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
     using C = DecCfg<D, I8, GH>;
     const int esz = I8 ? 1 : 2;
     const CUtensorMapDataType kvt = I8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const bool paged = L.page_table != nullptr;
+    if constexpr (!I8 && D != 256) {
+        // both contractions on the tensor cores where the boxes allow it:
+        // 16-row boxes must not cross a page, and cover at most Hkv heads
+        int nh = 1;
+        while (nh < plan.nh_box) nh <<= 1;
+        if ((!paged || L.page_size % 16 == 0) && nh <= L.Hkv) {
+            switch (nh) {
+                case 1: return launch_decode_tc<D, 1>(L, plan);
+                case 2: return launch_decode_tc<D, 2>(L, plan);
+                case 4: return launch_decode_tc<D, 4>(L, plan);
+                default: return launch_decode_tc<D, 8>(L, plan);
+            }
+        }
+    }
     const int R = paged ? (L.page_size < C::T ? L.page_size : C::T) : C::T;
     CUtensorMap tk, tv, tks, tvs;
     attn_status st;
@@ -692,48 +799,11 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
             return set_error(ATTN_ECUDA, "cudaFuncSetAttribute(decode smem) failed");
         attr_set[dev] = true;
     }
-    const int cap_layout = paged ? L.max_pages * L.page_size : L.max_kv;
-    DecArgs a;
-    a.q = static_cast<const __half*>(L.q);
-    a.kv_len = L.kv_len;
-    a.page_table = L.page_table;
-    uint8_t* ws = static_cast<uint8_t*>(L.workspace);
-    a.ws_prefix = reinterpret_cast<int32_t*>(ws);
-    a.ws_lse = reinterpret_cast<float*>(ws + plan.off_lse);
-    a.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
-    a.B = L.B;
-    a.Hq = L.Hq;
-    a.Hkv = L.Hkv;
-    a.G = L.Hq / L.Hkv;
-    a.HG = plan.HG;
-    a.U = L.Hkv * plan.HG;
-    a.n_hb = plan.n_hb;
-    a.nh_box = plan.nh_box;
-    a.split = plan.split;
-    a.cap_eff = cap_layout < L.max_kv ? cap_layout : L.max_kv;
-    a.window = L.window;
-    a.P = paged ? L.page_size : 0;
-    a.R = R;
-    a.max_pages = L.max_pages;
-    a.n_pages = paged ? L.n_pages : 0;
-    a.paged = paged;
-    const bool capped = L.softcap > 0.f;
-    a.qscale = capped ? L.scale / L.softcap : L.scale * kLog2e;
-    a.cap_log2 = capped ? L.softcap * kLog2e : 0.f;
-    a.err = L.err_word;
-    long grid = sm_count();
-    if (plan.max_items < grid) grid = plan.max_items;
-    if (grid < 1) grid = 1;
-    decode_split_kernel<D, I8, GH><<<(unsigned)grid, kDecThreads, C::SMEM_ALLOC, L.stream>>>(tk, tv, tks, tvs, a);
-    cudaError_t e = cudaGetLastError();
+    const DecArgs a = make_dec_args(L, plan, R);
+    decode_split_kernel<D, I8, GH><<<decode_grid(plan), kDecThreads, C::SMEM_ALLOC, L.stream>>>(tk, tv, tks, tvs, a);
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode split launch failed: %s", cudaGetErrorString(e));
-    const int nwarps = L.B * L.Hq;
-    decode_combine_kernel<D><<<(nwarps + 3) / 4, 128, 0, L.stream>>>(
-        L.kv_len, a.ws_prefix, a.ws_lse, a.ws_o, static_cast<__half*>(L.out), L.lse, L.B, L.Hq, a.G, GH, plan.HG,
-        plan.split, a.cap_eff, L.window);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode combine launch failed: %s", cudaGetErrorString(e));
-    return ATTN_OK;
+    return launch_combine<D>(L, plan, a);
 }
 
 template <int D, bool I8>

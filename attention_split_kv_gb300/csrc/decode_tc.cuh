@@ -1,0 +1,486 @@
+// decode_tc.cuh -- split-KV decode with both contractions on the tcgen05
+// tensor cores (f16 caches, head_dim 64 or 128, contiguous or paged with
+// pages of a multiple of 16 tokens).  Included by decode.cu, whose work-item
+// enumeration (sequence, head block, split), partial-row workspace and
+// log-sum-exp combine pass it shares; only the per-split kernel differs.
+//
+// Same computation as decode_split_kernel (doppler attention.js, the decode
+// variants of executeAttention): for each query head h of kv head g, softmax
+// over the kept keys of scale * q_h . k_j applied to v_j, here accumulated per
+// split with an online softmax and merged across splits by the combine pass.
+//
+// A work item covers the up-to-32 query heads of one head block.  Each TMA
+// box holds 16 tokens x NH kv heads x 64 dims of K (or V) with the 128-byte
+// swizzle, so NBX = 8 / NH boxes of consecutive 16-token groups stack into a
+// 128-row operand whose row m is (token m / NH, kv head m % NH):
+//
+//   S   = Q' K^T   M=128 (rows 0-31: the block's query heads), N=128 rows of
+//                  the tile, K=D; f32 in TMEM, double-buffered
+//   P   = exp2(S * scale * log2 e - m)  one thread of warp 0 per query head:
+//                  it keeps the entries of its own kv head (every NH-th
+//                  column), zeros the rest, and writes the row to TMEM as f16
+//   O  += P V      M=128, N=D, K=128 (P from TMEM, V in shared memory as the
+//                  MN-major operand): P is zero off its kv head, so each
+//                  query head only sums its own head's values
+//
+// Rows 32-127 of S/P/O are never read.  Roles (96 threads): warp 0 softmax +
+// per-split epilogue, warp 1 TMA producer, warp 2 TMEM allocator + MMA issuer.
+// Keys outside the split (window start, sequence end, boxes never loaded) are
+// masked in the softmax, and their V rows are zeroed in shared memory before
+// the PV product so that stale or unwritten cache contents never reach it.
+
+namespace tcdec {
+
+constexpr int kThreads = 96;
+constexpr int TR = 128;                       // rows of the K/V operand per MMA tile
+constexpr int QROWS = 32;                     // query rows written (NW units x up to 4 heads)
+
+template <int D>
+struct Cfg {
+    static constexpr int NCH = D / 64;                         // 64-dim (128-byte) chunks
+    static constexpr uint32_t CHUNK = TR * 128;                // one chunk of a K or V tile
+    static constexpr uint32_t KV_BYTES = NCH * CHUNK;          // one K (or V) tile
+    static constexpr uint32_t QCH = QROWS * 128;               // one chunk of Q' (32 rows)
+    static constexpr uint32_t QBUF = NCH * QCH;
+    static constexpr uint32_t OFF_Q = 0;                       // two Q' buffers
+    static constexpr uint32_t OFF_RING = 2 * QBUF;             // the MMA reads 128 rows from a Q'
+    // chunk; rows 32-127 run on into the rings (never used), so the K ring must
+    // hold at least 96 more rows of 128 bytes after the last Q' chunk.
+    // Separate K and V rings: a K tile is released once its QK^T has run, a V
+    // tile once its PV has run, so K loads run further ahead.
+    static constexpr int NTILE_RAW = (int)((226u * 1024u - OFF_RING - 1024u - 4096u) / KV_BYTES);
+    static constexpr int NK = (NTILE_RAW / 2) > 6 ? 6 : NTILE_RAW / 2;   // K ring slots
+    static constexpr int NV = NK;                                      // V ring slots
+    static constexpr uint32_t OFF_VRING = OFF_RING + NK * KV_BYTES;
+    static constexpr uint32_t OFF_BARS = OFF_VRING + NV * KV_BYTES;
+    // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_full[2], s_full[2],
+    // p_full[2], pv_done[2], o_free, teardown
+    static constexpr int N_BARS = 2 * NK + 2 * NV + 10;
+    static constexpr uint32_t OFF_PREFIX = OFF_BARS + N_BARS * 8;
+    static constexpr uint32_t PREFIX_BYTES = ((kDecodeMaxBatch + 1) * 4 + 127) / 128 * 128;
+    static constexpr uint32_t OFF_MISC = OFF_PREFIX + PREFIX_BYTES;   // scan scratch, abort flag, TMEM base
+    static constexpr uint32_t SMEM_USED = OFF_MISC + 256;
+    static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+    // TMEM columns: S[2] (128 each), P[2] (64 each: 128 f16 keys), O (D)
+    static constexpr uint32_t COL_S = 0, COL_P = 256, COL_O = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(COL_O + D <= TMEM_COLS, "TMEM budget");
+    static_assert(NK >= 2 && NV >= 2, "rings too small");
+    static_assert(NK * KV_BYTES >= 3 * QCH, "Q' overrun stays inside the K ring");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+};
+
+// the NH candidates c[0..NH) -> c[sel] with a select tree on the bits of sel
+template <int NH>
+__device__ __forceinline__ float pick(const uint32_t* c, int sel) {
+    if constexpr (NH == 1) {
+        return __uint_as_float(c[0]);
+    } else if constexpr (NH == 2) {
+        return __uint_as_float((sel & 1) ? c[1] : c[0]);
+    } else if constexpr (NH == 4) {
+        const uint32_t a0 = (sel & 1) ? c[1] : c[0], a1 = (sel & 1) ? c[3] : c[2];
+        return __uint_as_float((sel & 2) ? a1 : a0);
+    } else {
+        const uint32_t a0 = (sel & 1) ? c[1] : c[0], a1 = (sel & 1) ? c[3] : c[2];
+        const uint32_t a2 = (sel & 1) ? c[5] : c[4], a3 = (sel & 1) ? c[7] : c[6];
+        const uint32_t b0 = (sel & 2) ? a1 : a0, b1 = (sel & 2) ? a3 : a2;
+        return __uint_as_float((sel & 4) ? b1 : b0);
+    }
+}
+
+// The CTA's tiles in issue order: work items it = blockIdx.x, +gridDim.x, ...,
+// each cut into MMA tiles of NBX 16-token groups.
+struct Cursor {
+    int it, idx, mt, n_mt;   // item, its index within this CTA, MMA tile within it, tiles in it
+    Item I;
+};
+
+template <int NBX>
+__device__ __forceinline__ void cursor_load(Cursor& c, int total, const int* pref, const DecArgs& A) {
+    c.mt = 0;
+    c.n_mt = 0;
+    if (c.it < total) {
+        c.I = decode_item<16>(c.it, pref, A);
+        c.n_mt = (c.I.ntile + NBX - 1) / NBX;
+    }
+}
+template <int NBX>
+__device__ __forceinline__ void cursor_start(Cursor& c, int total, const int* pref, const DecArgs& A) {
+    c.it = blockIdx.x;
+    c.idx = 0;
+    cursor_load<NBX>(c, total, pref, A);
+    while (c.it < total && c.n_mt == 0) {   // items without tiles hold no keys
+        c.it += gridDim.x;
+        ++c.idx;
+        cursor_load<NBX>(c, total, pref, A);
+    }
+}
+template <int NBX>
+__device__ __forceinline__ void cursor_next(Cursor& c, int total, const int* pref, const DecArgs& A) {
+    if (++c.mt < c.n_mt) return;
+    do {
+        c.it += gridDim.x;
+        ++c.idx;
+        cursor_load<NBX>(c, total, pref, A);
+    } while (c.it < total && c.n_mt == 0);
+}
+
+template <int D, int NH>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 const DecArgs A) {
+    using C = Cfg<D>;
+    constexpr int NCH = C::NCH, NK = C::NK, NV = C::NV;
+    constexpr int NBX = 8 / NH;                 // 16-token boxes per MMA tile
+    constexpr int TT = TR / NH;                 // tokens per MMA tile
+    constexpr uint32_t BOXB = 16 * NH * 128;    // bytes of one box (one chunk)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+    int* pref = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
+    int* scratch = reinterpret_cast<int*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 128);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 132);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    const int B_KFULL = 0, B_KEMPTY = NK, B_VFULL = 2 * NK, B_VEMPTY = 2 * NK + NV, B_QFULL = 2 * NK + 2 * NV,
+              B_SFULL = B_QFULL + 2, B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 2, B_OFREE = B_PVDONE + 2,
+              B_TEARDOWN = B_OFREE + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(bar(B_KFULL + s), 1);
+            mbar_init(bar(B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(bar(B_VFULL + s), 1);
+            mbar_init(bar(B_VEMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_QFULL + b), 32);
+            mbar_init(bar(B_SFULL + b), 1);
+            mbar_init(bar(B_PFULL + b), 32);
+            mbar_init(bar(B_PVDONE + b), 1);
+        }
+        mbar_init(bar(B_OFREE), 32);
+        mbar_init(bar(B_TEARDOWN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    build_prefix(A, pref, scratch);   // ends with __syncthreads
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int total = pref[A.B];
+    if (blockIdx.x == 0) {
+        for (int b = threadIdx.x; b <= A.B; b += blockDim.x) A.ws_prefix[b] = pref[b];
+    }
+
+    if (warp == 1) {
+        // ------------------------------------------------------------ TMA producers
+        // lane 0 loads the K tiles, lane 1 the V tiles; each waits only for its
+        // own ring
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+            const int NS = is_k ? NK : NV;
+            const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
+            const uint32_t ring = sbase + (is_k ? C::OFF_RING : C::OFF_VRING);
+            tma_prefetch_desc(tm);
+            Cursor c;
+            cursor_start<NBX>(c, total, pref, A);
+            uint32_t j = 0;
+            bool ok = true;
+            for (; c.it < total; cursor_next<NBX>(c, total, pref, A), ++j) {
+                const int slot = j % NS;
+                if (j >= (uint32_t)NS &&
+                    !mbar_wait(bar(b_empty + slot), ((j / NS) - 1) & 1, abort_flag, A.err, kErrTimeoutSlot)) {
+                    ok = false;
+                    break;
+                }
+                const int g0 = (c.I.hb * NW) / A.HG;
+                const int nbox = min(NBX, c.I.ntile - c.mt * NBX);
+                mbar_arrive_expect_tx(bar(b_full + slot), nbox * NCH * BOXB);
+                for (int bx = 0; bx < nbox; ++bx) {
+                    const int t0 = c.I.ks + (c.mt * NBX + bx) * 16;
+                    int page = c.I.b, row = t0;
+                    if (A.paged) {
+                        page = __ldg(&A.page_table[(size_t)c.I.b * A.max_pages + t0 / A.P]);
+                        if (page < 0 || page >= A.n_pages) {
+                            // a page id outside the pool: read page 0 instead and report it
+                            atomicExch(A.err, kErrBadPage);
+                            page = 0;
+                        }
+                        row = t0 % A.P;
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch)
+                        tma_load_4d(ring + slot * C::KV_BYTES + ch * C::CHUNK + bx * BOXB, tm, bar(b_full + slot),
+                                    ch * 64, g0, row, page);
+                }
+            }
+            if (!ok) {
+                // let copies in flight land before shared memory is released
+                volatile int never = 0;
+                const uint32_t first = j > (uint32_t)NS ? j - NS : 0;
+                for (uint32_t x = first; x < j; ++x)
+                    mbar_wait(bar(b_full + (x % NS)), (x / NS) & 1, &never, A.err, kErrTimeoutLoad);
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f16_f32(128, TR, false);
+            constexpr uint32_t idesc_o = idesc_f16_f32(128, D, true);
+            Cursor cs, cp;                    // next S to issue, next PV to issue
+            cursor_start<NBX>(cs, total, pref, A);
+            cursor_start<NBX>(cp, total, pref, A);
+            uint32_t js = 0;                  // tiles whose S has been issued
+            bool ok = true;
+            // S_j: Q' of its item (buffer idx & 1) times the K tile of slot j
+            auto issue_s = [&]() -> bool {
+                const int slot = js % NK;
+                if (cs.mt == 0 &&
+                    !mbar_wait(bar(B_QFULL + (cs.idx & 1)), (cs.idx >> 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax))
+                    return false;
+                if (!mbar_wait(bar(B_KFULL + slot), (js / NK) & 1, abort_flag, A.err, kErrTimeoutLoad)) return false;
+                tc_fence_after();
+                const uint32_t qb = sbase + C::OFF_Q + (cs.idx & 1) * C::QBUF;
+                const uint32_t kb = sbase + C::OFF_RING + slot * C::KV_BYTES;
+                const uint32_t d_tmem = tmem + C::COL_S + (js & 1) * 128;
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = smem_desc_sw128(qb + ch * C::QCH + kk * 32, 16, 1024);
+                        const uint64_t b = smem_desc_sw128(kb + ch * C::CHUNK + kk * 32, 16, 1024);
+                        tc_mma_f16_ss(d_tmem, a, b, idesc_s, (ch | kk) != 0);
+                    }
+                tc_commit(bar(B_SFULL + (js & 1)));
+                tc_commit(bar(B_KEMPTY + slot));
+                ++js;
+                cursor_next<NBX>(cs, total, pref, A);
+                return true;
+            };
+            if (cs.it < total) ok = issue_s();
+            for (uint32_t j = 0; ok && cp.it < total; ++j, cursor_next<NBX>(cp, total, pref, A)) {
+                // S_{j+1} first (its buffer was last read by softmax j-1, whose P we
+                // waited for below in the previous iteration), so QK^T of the next
+                // tile overlaps the softmax of this one
+                if (cs.it < total && !(ok = issue_s())) break;
+                if (!mbar_wait(bar(B_PFULL + (j & 1)), (j >> 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax)) break;
+                // the first PV of an item overwrites O: the epilogue of the previous
+                // item must have read it
+                if (cp.mt == 0 && cp.idx > 0 &&
+                    !mbar_wait(bar(B_OFREE), (cp.idx - 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax))
+                    break;
+                const int slot = j % NV;
+                if (!mbar_wait(bar(B_VFULL + slot), (j / NV) & 1, abort_flag, A.err, kErrTimeoutLoad)) break;
+                tc_fence_after();
+                const uint32_t vb = sbase + C::OFF_VRING + slot * C::KV_BYTES;
+                const uint32_t p_tmem = tmem + C::COL_P + (j & 1) * 64;
+#pragma unroll
+                for (int kk = 0; kk < TR / 16; ++kk) {
+                    // 16 rows per MMA: 8 TMEM columns of P, 16 rows of V (2048 bytes)
+                    const uint64_t b = smem_desc_sw128(vb + kk * 16 * 128, C::CHUNK, 1024);
+                    tc_mma_f16_ts(tmem + C::COL_O, p_tmem + kk * 8, b, idesc_o, (cp.mt > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(B_PVDONE + (j & 1)));
+                tc_commit(bar(B_VEMPTY + slot));
+            }
+            // all issued MMAs must retire before TMEM is released
+            tc_commit(bar(B_TEARDOWN));
+            volatile int never = 0;
+            mbar_wait(bar(B_TEARDOWN), 0, &never, A.err, kErrTimeoutMma);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax (warp 0)
+        const int r = lane;                         // query row = TMEM lane
+        const int GH = A.G / A.HG;                  // query heads per unit
+        const int wu = r / GH, hs = r - wu * GH;    // unit of the head block, head inside it
+        const uint32_t lane_base = tmem;            // warp 0: TMEM lanes 0-31
+
+        // Q' rows of item `cur` into buffer idx & 1 (row r: this thread's query head)
+        auto build_q = [&](const Cursor& cur) {
+            const uint32_t qb = C::OFF_Q + (cur.idx & 1) * C::QBUF;
+            const int u = cur.I.hb * NW + wu;
+            const bool act = wu < NW && r < NW * GH && u < A.U;
+            const int g = u / A.HG, hg = u - g * A.HG;
+            const __half* qrow = A.q + ((size_t)cur.I.b * A.Hq + g * A.G + hg * GH + hs) * D;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (act) v = *reinterpret_cast<const uint4*>(qrow + ch * 64 + x * 8);
+                    *reinterpret_cast<uint4*>(smem + qb + ch * C::QCH + r * 128 + ((x ^ (r & 7)) << 4)) = v;
+                }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(B_QFULL + (cur.idx & 1)));
+        };
+
+        Cursor c;
+        cursor_start<NBX>(c, total, pref, A);
+        if (c.it < total) {
+            build_q(c);
+            Cursor n = c;
+            n.mt = n.n_mt - 1;
+            cursor_next<NBX>(n, total, pref, A);
+            if (n.it < total) build_q(n);
+        }
+        uint32_t j = 0;
+        bool ok = true;
+        while (ok && c.it < total) {
+            const Cursor item = c;                  // this item
+            if (item.idx > 0) {
+                // Q' of the item after this one, into the buffer the previous item used
+                // (all of its S products have been consumed)
+                Cursor n = item;
+                n.mt = n.n_mt - 1;
+                cursor_next<NBX>(n, total, pref, A);
+                if (n.it < total) build_q(n);
+            }
+            const int u = item.I.hb * NW + wu;
+            const bool act = wu < NW && r < NW * GH && u < A.U;
+            const int g = act ? u / A.HG : 0;
+            const int gl = act ? g - (item.I.hb * NW) / A.HG : 0;   // kv head inside the tile (row % NH)
+            float m_used = -INFINITY, l_sum = 0.f;
+            uint32_t j_last = j;
+            for (int mt = 0; mt < item.n_mt; ++mt, ++j) {
+                j_last = j;
+                if (!mbar_wait(bar(B_SFULL + (j & 1)), (j >> 1) & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
+                tc_fence_after();
+                float s[TT];
+                {
+                    uint32_t v[TR];
+#pragma unroll
+                    for (int q = 0; q < TR / 32; ++q)
+                        tc_ld_32x32b_x32(lane_base + C::COL_S + (j & 1) * 128 + q * 32,
+                                         *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
+                    tc_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < TT; ++t) s[t] = pick<NH>(v + t * NH, gl);
+                }
+                const int t0 = item.I.ks + mt * TT;
+                const int v_lo = max(item.I.start - t0, 0);
+                const int v_hi = min(item.I.ke - t0, TT);
+                float mx = -INFINITY;
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    float x = s[t] * A.qscale;
+                    if (A.cap_log2 > 0.f) x = A.cap_log2 * tanh_abs_accurate(x);
+                    x = (t >= v_lo && t < v_hi) ? x : -INFINITY;
+                    s[t] = x;
+                    mx = fmaxf(mx, x);
+                }
+                const bool need = mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx > -INFINITY);
+                const bool rescale = __any_sync(0xffffffffu, need) && mt > 0;
+                float alpha = 1.f;
+                if (need) {
+                    const float m_new = fmaxf(mx, m_used);
+                    alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
+                    l_sum *= alpha;
+                    m_used = m_new;
+                }
+                const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
+                uint32_t pw[64];                    // the P row: 128 f16 entries
+                float ls = 0.f;
+                if constexpr (NH == 1) {
+#pragma unroll
+                    for (int t = 0; t < TT; t += 2) {
+                        const float p0 = ex2_approx(s[t] - m_off), p1 = ex2_approx(s[t + 1] - m_off);
+                        ls += p0 + p1;
+                        const __half2 h2 = __floats2half2_rn(p0, p1);
+                        pw[t / 2] = act ? *reinterpret_cast<const uint32_t*>(&h2) : 0u;
+                    }
+                } else {
+                    const int hp = gl >> 1;
+#pragma unroll
+                    for (int t = 0; t < TT; ++t) {
+                        const float p = ex2_approx(s[t] - m_off);
+                        ls += p;
+                        const uint32_t h = __half_as_ushort(__float2half_rn(p));
+                        const uint32_t word = act ? ((gl & 1) ? (h << 16) : h) : 0u;
+#pragma unroll
+                        for (int w = 0; w < NH / 2; ++w) pw[t * (NH / 2) + w] = (w == hp) ? word : 0u;
+                    }
+                }
+                l_sum += ls;
+                if (rescale) {
+                    // O must not be in flight while it is rescaled
+                    if (!mbar_wait(bar(B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        tc_ld_32x32b_x32(lane_base + C::COL_O + q * 32, o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tc_st_32x32b_x32(lane_base + C::COL_O + q * 32, o);
+                    }
+                }
+                // P buffer j & 1 was last read by PV_{j-2}
+                if (j >= 2 && !mbar_wait(bar(B_PVDONE + (j & 1)), ((j - 2) >> 1) & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
+                tc_st_32x32b_x32(lane_base + C::COL_P + (j & 1) * 64, *reinterpret_cast<const uint32_t(*)[32]>(pw));
+                tc_st_32x32b_x32(lane_base + C::COL_P + (j & 1) * 64 + 32, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32));
+                if (v_lo > 0 || v_hi < TT) {
+                    // zero the V rows of masked tokens (all NH heads, every chunk), once
+                    // the tile's copy has landed
+                    if (!mbar_wait(bar(B_VFULL + (j % NV)), (j / NV) & 1, abort_flag, A.err, kErrTimeoutLoad)) { ok = false; break; }
+                    uint8_t* vt = smem + C::OFF_VRING + (j % NV) * C::KV_BYTES;
+                    const int lo_end = max(v_lo, 0) * NH * 128, hi_beg = max(v_hi, 0) * NH * 128;
+#pragma unroll 1
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        uint8_t* cb = vt + ch * C::CHUNK;
+                        for (int o = lane * 16; o < lo_end; o += 32 * 16) *reinterpret_cast<uint4*>(cb + o) = make_uint4(0u, 0u, 0u, 0u);
+                        for (int o = hi_beg + lane * 16; o < (int)C::CHUNK; o += 32 * 16)
+                            *reinterpret_cast<uint4*>(cb + o) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(B_PFULL + (j & 1)));
+            }
+            if (!ok) break;
+            // ---- end of the split: (lse, o / l) of this thread's query head
+            ok = mbar_wait(bar(B_PVDONE + (j_last & 1)), (j_last >> 1) & 1, abort_flag, A.err, kErrTimeoutMma);
+            if (!ok) break;
+            tc_fence_after();
+            const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+            const size_t prow = ((size_t)item.it * NW + wu) * GH + hs;
+#pragma unroll 1
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tc_ld_32x32b_x32(lane_base + C::COL_O + q * 32, o);
+                tc_wait_ld();
+                if (act) {
+                    float4* dst = reinterpret_cast<float4*>(A.ws_o + prow * D + q * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                             __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                }
+            }
+            if (act) A.ws_lse[prow] = l_sum > 0.f ? m_used + __log2f(l_sum) : -INFINITY;
+            tc_fence_before();
+            mbar_arrive(bar(B_OFREE));
+            c = item;
+            c.mt = c.n_mt - 1;
+            cursor_next<NBX>(c, total, pref, A);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace tcdec

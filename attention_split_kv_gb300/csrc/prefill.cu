@@ -156,18 +156,6 @@ __device__ __forceinline__ float row_max(const float (&t)[N]) {
     return fmaxf(max3(a[0], a[1], a[2]), max3(a[3], a[4], fmaxf(a[5], max3(a[6], a[7], a[0]))));
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A is read from TMEM (lane =
-// row, each 32-bit column holds two consecutive f16 elements of K).
-__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 struct PrefillArgs {
     __half* out;
     float* lse;

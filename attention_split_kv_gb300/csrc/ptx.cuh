@@ -144,6 +144,18 @@ __device__ __forceinline__ void tc_mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, 
 
 // Arrive (once) on an mbarrier when all previously issued tcgen05 async
 // operations of this thread have completed.
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A is read from TMEM (lane =
+// row, each 32-bit column holds two consecutive f16 elements of K).
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");

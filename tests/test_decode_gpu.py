@@ -70,11 +70,19 @@ def test_decode_paged(page_size, int8):
 @pytest.mark.parametrize("int8", [False, True], ids=["f16", "int8"])
 @pytest.mark.parametrize("page_size", [8, 16, 32])
 def test_paged_is_bit_identical_to_contiguous(page_size, int8):
+    # the page table only changes where rows are read from: the same kernel
+    # gives the same bits.  f16 caches with pages of a multiple of 16 tokens run
+    # the tensor-core kernel like the contiguous cache; pages of 8 f16 tokens run
+    # the CUDA-core kernel, which rounds differently, so there the two agree to
+    # the parity tolerance instead.
     case = si.make_decode_case(3, 8, 2, 128, [5, 450, 300], seed=41, int8=int8, cap=456)
     paged = si.paged_from_contiguous(case, page_size, seed=42)
     a, la = _run(case, split_keys=64, max_kv=456)
     b, lb = _run(paged, split_keys=64, max_kv=456)
-    assert np.array_equal(a, b) and np.array_equal(la, lb)
+    if int8 or page_size % 16 == 0:
+        assert np.array_equal(a, b) and np.array_equal(la, lb)
+    else:
+        assert np.abs(a - b).max() <= 2e-3 and np.abs(la - lb).max() <= 1e-3
 
 
 @pytest.mark.parametrize("window", [1, 5, 16, 100, 5000])
