@@ -702,8 +702,17 @@ template <int D, int NH>
 attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan) {
     using C = tcdec::Cfg<D>;
     const bool paged = L.page_table != nullptr;
-    CUtensorMap tk, tv;
+    CUtensorMap tq, tk, tv;
     attn_status st;
+    const int q_rows = L.Hq < tcdec::QROWS ? L.Hq : tcdec::QROWS;
+    {
+        // q [B][Hq][D]: boxes of (64 dims, q_rows heads, 1), 128-byte swizzle
+        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)L.Hq, (uint64_t)L.B};
+        const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * L.Hq};
+        const uint32_t box[3] = {64u, (uint32_t)q_rows, 1u};
+        if ((st = encode_tmap_sw128(&tq, L.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, dims, strides, box)) != ATTN_OK)
+            return st;
+    }
     {
         // [pages or B][rows][Hkv][D]: boxes of (64 dims, NH heads, 16 rows, 1), 128-byte swizzle
         uint64_t dims[4], strides[3];
@@ -730,7 +739,8 @@ attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan) {
         attr_set[dev] = true;
     }
     const DecArgs a = make_dec_args(L, plan, 16);
-    tcdec::decode_tc_kernel<D, NH><<<decode_grid(plan), tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tk, tv, a);
+    tcdec::decode_tc_kernel<D, NH><<<decode_grid(plan), tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a,
+                                                                                                    q_rows);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode tc launch failed: %s", cudaGetErrorString(e));
     return launch_combine<D>(L, plan, a);

@@ -14,8 +14,8 @@
 // swizzle, so NBX = 8 / NH boxes of consecutive 16-token groups stack into a
 // 128-row operand whose row m is (token m / NH, kv head m % NH):
 //
-//   S   = Q' K^T   M=128 (rows 0-31: the block's query heads), N=128 rows of
-//                  the tile, K=D; f32 in TMEM, double-buffered
+//   S   = Q' K^T   M=128 (rows 0-31: the block's query heads, loaded by TMA
+//                  from q), N=128 rows of the tile, K=D; f32 in TMEM
 //   P   = exp2(S * scale * log2 e - m)  one thread of warp 0 per query head:
 //                  it keeps the entries of its own kv head (every NH-th
 //                  column), zeros the rest, and writes the row to TMEM as f16
@@ -24,7 +24,11 @@
 //                  query head only sums its own head's values
 //
 // Rows 32-127 of S/P/O are never read.  Roles (96 threads): warp 0 softmax +
-// per-split epilogue, warp 1 TMA producer, warp 2 TMEM allocator + MMA issuer.
+// per-split epilogue, warp 1 TMA producers (lane 0: Q' and K, lane 1: V),
+// warp 2 TMEM allocator + MMA issuer.  S has one TMEM buffer, released as soon
+// as the softmax holds its row in registers, so the next QK^T still overlaps
+// the exponentials; P and O have two, and the epilogue of a split runs after
+// the first tile of the next one, so no MMA waits for it.
 // Keys outside the split (window start, sequence end, boxes never loaded) are
 // masked in the softmax, and their V rows are zeroed in shared memory before
 // the PV product so that stale or unwritten cache contents never reach it.
@@ -53,18 +57,18 @@ struct Cfg {
     static constexpr int NV = NK;                                      // V ring slots
     static constexpr uint32_t OFF_VRING = OFF_RING + NK * KV_BYTES;
     static constexpr uint32_t OFF_BARS = OFF_VRING + NV * KV_BYTES;
-    // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_full[2], s_full[2],
-    // p_full[2], pv_done[2], o_free, teardown
-    static constexpr int N_BARS = 2 * NK + 2 * NV + 10;
+    // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_full[2], q_empty[2],
+    // s_full, s_free, p_full[2], pv_done[2], o_free[2], teardown
+    static constexpr int N_BARS = 2 * NK + 2 * NV + 15;
     static constexpr uint32_t OFF_PREFIX = OFF_BARS + N_BARS * 8;
     static constexpr uint32_t PREFIX_BYTES = ((kDecodeMaxBatch + 1) * 4 + 127) / 128 * 128;
     static constexpr uint32_t OFF_MISC = OFF_PREFIX + PREFIX_BYTES;   // scan scratch, abort flag, TMEM base
     static constexpr uint32_t SMEM_USED = OFF_MISC + 256;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-    // TMEM columns: S[2] (128 each), P[2] (64 each: 128 f16 keys), O (D)
-    static constexpr uint32_t COL_S = 0, COL_P = 256, COL_O = 384;
+    // TMEM columns: S (128), P[2] (64 each: 128 f16 keys), O[2] (D each)
+    static constexpr uint32_t COL_S = 0, COL_P = 128, COL_O = 256;
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(COL_O + D <= TMEM_COLS, "TMEM budget");
+    static_assert(COL_O + 2 * D <= TMEM_COLS, "TMEM budget");
     static_assert(NK >= 2 && NV >= 2, "rings too small");
     static_assert(NK * KV_BYTES >= 3 * QCH, "Q' overrun stays inside the K ring");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -127,8 +131,8 @@ __device__ __forceinline__ void cursor_next(Cursor& c, int total, const int* pre
 
 template <int D, int NH>
 __global__ void __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 const DecArgs A) {
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const DecArgs A, const int q_rows) {
     using C = Cfg<D>;
     constexpr int NCH = C::NCH, NK = C::NK, NV = C::NV;
     constexpr int NBX = 8 / NH;                 // 16-token boxes per MMA tile
@@ -144,8 +148,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 132);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int B_KFULL = 0, B_KEMPTY = NK, B_VFULL = 2 * NK, B_VEMPTY = 2 * NK + NV, B_QFULL = 2 * NK + 2 * NV,
-              B_SFULL = B_QFULL + 2, B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 2, B_OFREE = B_PVDONE + 2,
-              B_TEARDOWN = B_OFREE + 1;
+              B_QEMPTY = B_QFULL + 2, B_SFULL = B_QEMPTY + 2, B_SFREE = B_SFULL + 1, B_PFULL = B_SFREE + 1,
+              B_PVDONE = B_PFULL + 2, B_OFREE = B_PVDONE + 2, B_TEARDOWN = B_OFREE + 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -158,12 +162,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             mbar_init(bar(B_VEMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(B_QFULL + b), 32);
-            mbar_init(bar(B_SFULL + b), 1);
+            mbar_init(bar(B_QFULL + b), 1);
+            mbar_init(bar(B_QEMPTY + b), 1);
             mbar_init(bar(B_PFULL + b), 32);
             mbar_init(bar(B_PVDONE + b), 1);
+            mbar_init(bar(B_OFREE + b), 32);
         }
-        mbar_init(bar(B_OFREE), 32);
+        mbar_init(bar(B_SFULL), 1);
+        mbar_init(bar(B_SFREE), 32);
         mbar_init(bar(B_TEARDOWN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -172,6 +178,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
         tmem_relinquish();
     }
+    tc_fence_before();
     build_prefix(A, pref, scratch);   // ends with __syncthreads
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
@@ -179,11 +186,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (blockIdx.x == 0) {
         for (int b = threadIdx.x; b <= A.B; b += blockDim.x) A.ws_prefix[b] = pref[b];
     }
+    const int GH = A.G / A.HG;                  // query heads per unit
+    const int QB = NW * GH;                     // query rows of a head block
 
     if (warp == 1) {
         // ------------------------------------------------------------ TMA producers
-        // lane 0 loads the K tiles, lane 1 the V tiles; each waits only for its
-        // own ring
+        // lane 0 loads Q' (once per item) and the K tiles, lane 1 the V tiles;
+        // each waits only for its own buffers
         if (lane < 2) {
             const bool is_k = lane == 0;
             const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
@@ -191,11 +200,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
             const uint32_t ring = sbase + (is_k ? C::OFF_RING : C::OFF_VRING);
             tma_prefetch_desc(tm);
+            if (is_k) tma_prefetch_desc(&tm_q);
             Cursor c;
             cursor_start<NBX>(c, total, pref, A);
             uint32_t j = 0;
+            int q_last[2] = {-1, -1};   // last item whose Q' was loaded into each buffer
             bool ok = true;
             for (; c.it < total; cursor_next<NBX>(c, total, pref, A), ++j) {
+                if (is_k && c.mt == 0) {
+                    // Q' of this item: query heads hb*QB .. +q_rows of sequence b
+                    const int qb = c.idx & 1;
+                    if (c.idx >= 2 &&
+                        !mbar_wait(bar(B_QEMPTY + qb), ((c.idx >> 1) - 1) & 1, abort_flag, A.err, kErrTimeoutSlot)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(B_QFULL + qb), NCH * q_rows * 128);
+                    q_last[qb] = c.idx;
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch)
+                        tma_load_3d(sbase + C::OFF_Q + qb * C::QBUF + ch * C::QCH, &tm_q, bar(B_QFULL + qb), ch * 64,
+                                    c.I.hb * QB, c.I.b);
+                }
                 const int slot = j % NS;
                 if (j >= (uint32_t)NS &&
                     !mbar_wait(bar(b_empty + slot), ((j / NS) - 1) & 1, abort_flag, A.err, kErrTimeoutSlot)) {
@@ -229,6 +255,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const uint32_t first = j > (uint32_t)NS ? j - NS : 0;
                 for (uint32_t x = first; x < j; ++x)
                     mbar_wait(bar(b_full + (x % NS)), (x / NS) & 1, &never, A.err, kErrTimeoutLoad);
+                for (int qb = 0; qb < 2; ++qb)
+                    if (q_last[qb] >= 0) mbar_wait(bar(B_QFULL + qb), (q_last[qb] >> 1) & 1, &never, A.err, kErrTimeoutLoad);
             }
         }
     } else if (warp == 2) {
@@ -241,42 +269,44 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             cursor_start<NBX>(cp, total, pref, A);
             uint32_t js = 0;                  // tiles whose S has been issued
             bool ok = true;
-            // S_j: Q' of its item (buffer idx & 1) times the K tile of slot j
+            // S_js: Q' of its item (buffer idx & 1) times the K tile of ring slot js
             auto issue_s = [&]() -> bool {
                 const int slot = js % NK;
                 if (cs.mt == 0 &&
-                    !mbar_wait(bar(B_QFULL + (cs.idx & 1)), (cs.idx >> 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax))
+                    !mbar_wait(bar(B_QFULL + (cs.idx & 1)), (cs.idx >> 1) & 1, abort_flag, A.err, kErrTimeoutLoad))
                     return false;
+                // the single S buffer: the softmax has tile js-1 in registers
+                if (js > 0 && !mbar_wait(bar(B_SFREE), (js - 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax)) return false;
                 if (!mbar_wait(bar(B_KFULL + slot), (js / NK) & 1, abort_flag, A.err, kErrTimeoutLoad)) return false;
                 tc_fence_after();
                 const uint32_t qb = sbase + C::OFF_Q + (cs.idx & 1) * C::QBUF;
                 const uint32_t kb = sbase + C::OFF_RING + slot * C::KV_BYTES;
-                const uint32_t d_tmem = tmem + C::COL_S + (js & 1) * 128;
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t a = smem_desc_sw128(qb + ch * C::QCH + kk * 32, 16, 1024);
                         const uint64_t b = smem_desc_sw128(kb + ch * C::CHUNK + kk * 32, 16, 1024);
-                        tc_mma_f16_ss(d_tmem, a, b, idesc_s, (ch | kk) != 0);
+                        tc_mma_f16_ss(tmem + C::COL_S, a, b, idesc_s, (ch | kk) != 0);
                     }
-                tc_commit(bar(B_SFULL + (js & 1)));
+                tc_commit(bar(B_SFULL));
                 tc_commit(bar(B_KEMPTY + slot));
+                if (cs.mt + 1 == cs.n_mt) tc_commit(bar(B_QEMPTY + (cs.idx & 1)));   // last S of the item
                 ++js;
                 cursor_next<NBX>(cs, total, pref, A);
                 return true;
             };
             if (cs.it < total) ok = issue_s();
             for (uint32_t j = 0; ok && cp.it < total; ++j, cursor_next<NBX>(cp, total, pref, A)) {
-                // S_{j+1} first (its buffer was last read by softmax j-1, whose P we
-                // waited for below in the previous iteration), so QK^T of the next
-                // tile overlaps the softmax of this one
+                // S_{j+1} first (it waits for the softmax to hold S_j), so QK^T of
+                // the next tile overlaps the exponentials of this one
                 if (cs.it < total && !(ok = issue_s())) break;
                 if (!mbar_wait(bar(B_PFULL + (j & 1)), (j >> 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax)) break;
-                // the first PV of an item overwrites O: the epilogue of the previous
-                // item must have read it
-                if (cp.mt == 0 && cp.idx > 0 &&
-                    !mbar_wait(bar(B_OFREE), (cp.idx - 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax))
+                const int ob = cp.idx & 1;
+                // the first PV of an item overwrites its O buffer: the epilogue of the
+                // item that used it before must have read it
+                if (cp.mt == 0 && cp.idx >= 2 &&
+                    !mbar_wait(bar(B_OFREE + ob), ((cp.idx >> 1) - 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax))
                     break;
                 const int slot = j % NV;
                 if (!mbar_wait(bar(B_VFULL + slot), (j / NV) & 1, abort_flag, A.err, kErrTimeoutLoad)) break;
@@ -287,7 +317,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 for (int kk = 0; kk < TR / 16; ++kk) {
                     // 16 rows per MMA: 8 TMEM columns of P, 16 rows of V (2048 bytes)
                     const uint64_t b = smem_desc_sw128(vb + kk * 16 * 128, C::CHUNK, 1024);
-                    tc_mma_f16_ts(tmem + C::COL_O, p_tmem + kk * 8, b, idesc_o, (cp.mt > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_f16_ts(tmem + C::COL_O + ob * D, p_tmem + kk * 8, b, idesc_o, (cp.mt > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(B_PVDONE + (j & 1)));
                 tc_commit(bar(B_VEMPTY + slot));
@@ -300,68 +330,67 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     } else {
         // ------------------------------------------------------------ softmax (warp 0)
         const int r = lane;                         // query row = TMEM lane
-        const int GH = A.G / A.HG;                  // query heads per unit
         const int wu = r / GH, hs = r - wu * GH;    // unit of the head block, head inside it
         const uint32_t lane_base = tmem;            // warp 0: TMEM lanes 0-31
 
-        // Q' rows of item `cur` into buffer idx & 1 (row r: this thread's query head)
-        auto build_q = [&](const Cursor& cur) {
-            const uint32_t qb = C::OFF_Q + (cur.idx & 1) * C::QBUF;
-            const int u = cur.I.hb * NW + wu;
-            const bool act = wu < NW && r < NW * GH && u < A.U;
-            const int g = u / A.HG, hg = u - g * A.HG;
-            const __half* qrow = A.q + ((size_t)cur.I.b * A.Hq + g * A.G + hg * GH + hs) * D;
+        // the split epilogue, run one tile late: (lse, o / l) of this thread's query head
+        struct Pending {
+            bool on, act;
+            int it, ob;
+            uint32_t j_last;
+            float m, l;
+        } pend;
+        pend.on = false;
+        auto epilogue = [&]() -> bool {
+            if (!mbar_wait(bar(B_PVDONE + (pend.j_last & 1)), (pend.j_last >> 1) & 1, abort_flag, A.err, kErrTimeoutMma))
+                return false;
+            tc_fence_after();
+            const float inv = pend.l > 0.f ? 1.0f / pend.l : 0.f;
+            const size_t prow = ((size_t)pend.it * NW + wu) * GH + hs;
+#pragma unroll 1
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tc_ld_32x32b_x32(lane_base + C::COL_O + pend.ob * D + q * 32, o);
+                tc_wait_ld();
+                if (pend.act) {
+                    float4* dst = reinterpret_cast<float4*>(A.ws_o + prow * D + q * 32);
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (act) v = *reinterpret_cast<const uint4*>(qrow + ch * 64 + x * 8);
-                    *reinterpret_cast<uint4*>(smem + qb + ch * C::QCH + r * 128 + ((x ^ (r & 7)) << 4)) = v;
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                             __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
                 }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(B_QFULL + (cur.idx & 1)));
+            }
+            if (pend.act) A.ws_lse[prow] = pend.l > 0.f ? pend.m + __log2f(pend.l) : -INFINITY;
+            tc_fence_before();
+            mbar_arrive(bar(B_OFREE + pend.ob));
+            pend.on = false;
+            return true;
         };
 
         Cursor c;
         cursor_start<NBX>(c, total, pref, A);
-        if (c.it < total) {
-            build_q(c);
-            Cursor n = c;
-            n.mt = n.n_mt - 1;
-            cursor_next<NBX>(n, total, pref, A);
-            if (n.it < total) build_q(n);
-        }
         uint32_t j = 0;
         bool ok = true;
         while (ok && c.it < total) {
-            const Cursor item = c;                  // this item
-            if (item.idx > 0) {
-                // Q' of the item after this one, into the buffer the previous item used
-                // (all of its S products have been consumed)
-                Cursor n = item;
-                n.mt = n.n_mt - 1;
-                cursor_next<NBX>(n, total, pref, A);
-                if (n.it < total) build_q(n);
-            }
+            const Cursor item = c;
             const int u = item.I.hb * NW + wu;
-            const bool act = wu < NW && r < NW * GH && u < A.U;
+            const bool act = wu < NW && r < QB && u < A.U;
             const int g = act ? u / A.HG : 0;
             const int gl = act ? g - (item.I.hb * NW) / A.HG : 0;   // kv head inside the tile (row % NH)
+            const int ob = item.idx & 1;
             float m_used = -INFINITY, l_sum = 0.f;
-            uint32_t j_last = j;
             for (int mt = 0; mt < item.n_mt; ++mt, ++j) {
-                j_last = j;
-                if (!mbar_wait(bar(B_SFULL + (j & 1)), (j >> 1) & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
+                if (!mbar_wait(bar(B_SFULL), j & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
                 tc_fence_after();
                 float s[TT];
                 {
                     uint32_t v[TR];
 #pragma unroll
                     for (int q = 0; q < TR / 32; ++q)
-                        tc_ld_32x32b_x32(lane_base + C::COL_S + (j & 1) * 128 + q * 32,
-                                         *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
+                        tc_ld_32x32b_x32(lane_base + C::COL_S + q * 32, *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
                     tc_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(bar(B_SFREE));         // S is in registers: the next QK^T may run
 #pragma unroll
                     for (int t = 0; t < TT; ++t) s[t] = pick<NH>(v + t * NH, gl);
                 }
@@ -373,7 +402,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 for (int t = 0; t < TT; ++t) {
                     float x = s[t] * A.qscale;
                     if (A.cap_log2 > 0.f) x = A.cap_log2 * tanh_abs_accurate(x);
-                    x = (t >= v_lo && t < v_hi) ? x : -INFINITY;
+                    x = (act && t >= v_lo && t < v_hi) ? x : -INFINITY;
                     s[t] = x;
                     mx = fmaxf(mx, x);
                 }
@@ -417,11 +446,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll 1
                     for (int q = 0; q < D / 32; ++q) {
                         uint32_t o[32];
-                        tc_ld_32x32b_x32(lane_base + C::COL_O + q * 32, o);
+                        tc_ld_32x32b_x32(lane_base + C::COL_O + ob * D + q * 32, o);
                         tc_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tc_st_32x32b_x32(lane_base + C::COL_O + q * 32, o);
+                        tc_st_32x32b_x32(lane_base + C::COL_O + ob * D + q * 32, o);
                     }
                 }
                 // P buffer j & 1 was last read by PV_{j-2}
@@ -433,7 +462,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     // the tile's copy has landed
                     if (!mbar_wait(bar(B_VFULL + (j % NV)), (j / NV) & 1, abort_flag, A.err, kErrTimeoutLoad)) { ok = false; break; }
                     uint8_t* vt = smem + C::OFF_VRING + (j % NV) * C::KV_BYTES;
-                    const int lo_end = max(v_lo, 0) * NH * 128, hi_beg = max(v_hi, 0) * NH * 128;
+                    const int lo_end = v_lo * NH * 128, hi_beg = v_hi * NH * 128;
 #pragma unroll 1
                     for (int ch = 0; ch < NCH; ++ch) {
                         uint8_t* cb = vt + ch * C::CHUNK;
@@ -446,34 +475,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 tc_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(B_PFULL + (j & 1)));
+                // the previous item's epilogue, now that this item's first P is out
+                if (pend.on && !epilogue()) { ok = false; break; }
             }
             if (!ok) break;
-            // ---- end of the split: (lse, o / l) of this thread's query head
-            ok = mbar_wait(bar(B_PVDONE + (j_last & 1)), (j_last >> 1) & 1, abort_flag, A.err, kErrTimeoutMma);
-            if (!ok) break;
-            tc_fence_after();
-            const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-            const size_t prow = ((size_t)item.it * NW + wu) * GH + hs;
-#pragma unroll 1
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t o[32];
-                tc_ld_32x32b_x32(lane_base + C::COL_O + q * 32, o);
-                tc_wait_ld();
-                if (act) {
-                    float4* dst = reinterpret_cast<float4*>(A.ws_o + prow * D + q * 32);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                             __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-                }
-            }
-            if (act) A.ws_lse[prow] = l_sum > 0.f ? m_used + __log2f(l_sum) : -INFINITY;
-            tc_fence_before();
-            mbar_arrive(bar(B_OFREE));
+            pend.on = true;
+            pend.act = act;
+            pend.it = item.it;
+            pend.ob = ob;
+            pend.j_last = j - 1;
+            pend.m = m_used;
+            pend.l = l_sum;
             c = item;
             c.mt = c.n_mt - 1;
             cursor_next<NBX>(c, total, pref, A);
         }
+        if (ok && pend.on) epilogue();
     }
     tc_fence_before();
     __syncthreads();
