@@ -89,6 +89,12 @@ struct DecArgs {
     int32_t* ws_prefix;
     float* ws_lse;
     float* ws_o;
+    // balanced tensor-core kernel only: tile prefix over sequences and the
+    // per-CTA fix-up partials (see decode_tc.cuh)
+    int32_t* ws_tpref;
+    int32_t* ws_fix_meta;
+    float* ws_fix_lse;
+    float* ws_fix_o;
     int B, Hq, Hkv, G, HG, U, n_hb, nh_box, split, cap_eff, window, P, R, max_pages, n_pages, paged;
     float qscale;      // multiplies q: scale*log2e (no cap) or scale/c (cap)
     float cap_log2;    // c*log2e, 0 when the cap is off
@@ -135,8 +141,9 @@ __device__ __forceinline__ Item decode_item(int it, const int* pref, const DecAr
     return r;
 }
 
-// Exclusive prefix over sequences of their work-item counts (block-wide scan).
-__device__ void build_prefix(const DecArgs& A, int* pref, int* scratch) {
+// Exclusive prefix over sequences of count(start, end) (block-wide scan).
+template <typename F>
+__device__ void build_prefix_of(const DecArgs& A, int* pref, int* scratch, F count) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nw = blockDim.x >> 5;
     int carry = 0;
@@ -146,7 +153,7 @@ __device__ void build_prefix(const DecArgs& A, int* pref, int* scratch) {
         if (b < A.B) {
             int start, end;
             seq_range(__ldg(&A.kv_len[b]), A.cap_eff, A.window, start, end);
-            v = A.n_hb * seq_splits(start, end, A.split);
+            v = count(start, end);
         }
         int x = v;
 #pragma unroll
@@ -173,6 +180,11 @@ __device__ void build_prefix(const DecArgs& A, int* pref, int* scratch) {
     }
     if (threadIdx.x == 0) pref[A.B] = carry;
     __syncthreads();
+}
+
+// Work items (sequence, head block, split) per sequence.
+__device__ void build_prefix(const DecArgs& A, int* pref, int* scratch) {
+    build_prefix_of(A, pref, scratch, [&](int start, int end) { return A.n_hb * seq_splits(start, end, A.split); });
 }
 
 // One lane's slice of a K or V row -> E floats (as E/2 pairs).
@@ -588,6 +600,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             if (lane == 0) A.ws_lse[prow + h] = lh > 0.f ? mh + __log2f(lh) : -INFINITY;
         }
     }
+    // this CTA's partials are written: the combine pass may be scheduled (it
+    // still waits for the whole grid to finish)
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
     if (warp == 0 && !ok && lane == 0) {
         // let copies in flight land before shared memory is released
         volatile int never = 0;
@@ -605,8 +620,12 @@ __global__ void __launch_bounds__(128)
 decode_combine_kernel(const int32_t* __restrict__ kv_len, const int32_t* __restrict__ ws_prefix,
                       const float* __restrict__ ws_lse, const float* __restrict__ ws_o, __half* __restrict__ out,
                       float* __restrict__ lse_out, int B, int Hq, int G, int GH, int HG, int split, int cap_eff,
-                      int window) {
+                      int window, const int32_t* __restrict__ fix_meta, const float* __restrict__ fix_lse,
+                      const float* __restrict__ fix_o, int n_fix, int n_hb) {
     constexpr int DPL = D / 32;   // dims per lane
+    // launched as a programmatic dependent of the split kernel: wait until that
+    // grid has finished and its partials are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (gw >= B * Hq) return;
@@ -617,26 +636,111 @@ decode_combine_kernel(const int32_t* __restrict__ kv_len, const int32_t* __restr
     seq_range(kv_len[b], cap_eff, window, start, end);
     const int ns = seq_splits(start, end, split);
     const int item0 = ws_prefix[b] + hb * ns;
+    auto lrow = [&](int sp) { return ((size_t)(item0 + sp) * NW + w) * GH + hs; };
+    const int fid = b * n_hb + hb;     // fix-up slots written for this (sequence, head block)
+    // the lse of the first KR*32 splits and every fix-up tag, as independent loads
+    // kept in registers (both passes below use them)
+    constexpr int KR = 4, KF = kDecodeMaxFix / 32;
+    float lsr[KR];
+#pragma unroll
+    for (int k = 0; k < KR; ++k) lsr[k] = (k * 32 + lane < ns) ? ws_lse[lrow(k * 32 + lane)] : -INFINITY;
+    bool mine[KF];
+#pragma unroll
+    for (int q = 0; q < KF; ++q) mine[q] = (q * 32 + lane < n_fix) && fix_meta[q * 32 + lane] == fid;
+    float fls[KF];
+#pragma unroll
+    for (int q = 0; q < KF; ++q) fls[q] = mine[q] ? fix_lse[((size_t)(q * 32 + lane) * NW + w) * GH + hs] : -INFINITY;
     float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, ws_lse[((size_t)(item0 + s) * NW + w) * GH + hs]);
+#pragma unroll
+    for (int k = 0; k < KR; ++k) M = fmaxf(M, lsr[k]);
+    for (int sp = KR * 32 + lane; sp < ns; sp += 32) M = fmaxf(M, ws_lse[lrow(sp)]);
+#pragma unroll
+    for (int q = 0; q < KF; ++q) M = fmaxf(M, fls[q]);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-    float wsum = 0.f;
-    if (M > -INFINITY) {
-        for (int s = 0; s < ns; ++s) {
-            const size_t row = ((size_t)(item0 + s) * NW + w) * GH + hs;
-            const float ls = ws_lse[row];
-            if (ls == -INFINITY) continue;
-            const float wt = ex2_approx(ls - M);
-            wsum += wt;
-            const float* src = ws_o + row * D + lane * DPL;
+    float wl_sum = 0.f;   // this lane's share of the weight sum
+    // DPL floats of a partial row (this lane's dims)
+    auto load_row = [&](const float* o_rows, size_t row, float (&v)[DPL]) {
+        const float* src = o_rows + row * D + lane * DPL;
+        if constexpr (DPL % 4 == 0) {
 #pragma unroll
-            for (int i = 0; i < DPL; ++i) acc[i] += wt * src[i];
+            for (int i = 0; i < DPL; i += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src + i);
+                v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < DPL; i += 2) {
+                const float2 x = *reinterpret_cast<const float2*>(src + i);
+                v[i] = x.x; v[i + 1] = x.y;
+            }
+        }
+    };
+    // acc += wt * v, as a select: rows whose lse is -inf were never written and
+    // may hold anything, so their (zero) weight must not multiply them
+    auto accumulate = [&](float wt, const float (&v)[DPL]) {
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] += (wt != 0.f) ? wt * v[i] : 0.f;
+    };
+    auto weight = [&](float ls) { return (ls == -INFINITY) ? 0.f : ex2_approx(ls - M); };
+    if (M > -INFINITY) {
+        // 32 splits at a time: lane l holds the weight of split base+l, then the
+        // warp reads the partial rows 8 at a time, all loads in flight together
+        for (int base = 0; base < ns; base += 32) {
+            const int k32 = base / 32;
+            float ls = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < KR; ++k)
+                if (k == k32) ls = lsr[k];
+            if (k32 >= KR && base + lane < ns) ls = ws_lse[lrow(base + lane)];
+            const float wl = weight(ls);
+            wl_sum += wl;
+            // the splits with weight (the rest were merged into another row or saw
+            // no key), read 8 at a time with all loads in flight together
+            unsigned mk = __ballot_sync(0xffffffffu, wl != 0.f);
+            while (mk) {
+                float v[8][DPL];
+                float wt[8];
+                const int k_first = __ffs(mk) - 1;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    int k = k_first;
+                    wt[q] = 0.f;
+                    if (mk) {
+                        k = __ffs(mk) - 1;
+                        mk &= mk - 1;
+                        wt[q] = __shfl_sync(0xffffffffu, wl, k);
+                    }
+                    load_row(ws_o, lrow(base + k), v[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) accumulate(wt[q], v[q]);
+            }
+        }
+        // the fix-up slots of this (sequence, head block)
+#pragma unroll
+        for (int q = 0; q < KF; ++q) {
+            const float wl = weight(fls[q]);
+            wl_sum += wl;
+            unsigned m = __ballot_sync(0xffffffffu, mine[q]);
+            while (m) {
+                const int k = __ffs(m) - 1;
+                m &= m - 1;
+                const float wt = __shfl_sync(0xffffffffu, wl, k);
+                if (wt != 0.f) {
+                    float v[DPL];
+                    load_row(fix_o, ((size_t)(q * 32 + k) * NW + w) * GH + hs, v);
+                    accumulate(wt, v);
+                }
+            }
         }
     }
+    float wsum = wl_sum;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
     __half* dst = out + ((size_t)b * Hq + h) * D + lane * DPL;
 #pragma unroll
@@ -657,6 +761,10 @@ DecArgs make_dec_args(const DecodeLaunch& L, const DecodePlan& plan, int R) {
     a.ws_prefix = reinterpret_cast<int32_t*>(ws);
     a.ws_lse = reinterpret_cast<float*>(ws + plan.off_lse);
     a.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
+    a.ws_tpref = reinterpret_cast<int32_t*>(ws + plan.off_tpref);
+    a.ws_fix_meta = reinterpret_cast<int32_t*>(ws + plan.off_fix_meta);
+    a.ws_fix_lse = reinterpret_cast<float*>(ws + plan.off_fix_lse);
+    a.ws_fix_o = reinterpret_cast<float*>(ws + plan.off_fix_o);
     a.B = L.B;
     a.Hq = L.Hq;
     a.Hkv = L.Hkv;
@@ -680,13 +788,32 @@ DecArgs make_dec_args(const DecodeLaunch& L, const DecodePlan& plan, int R) {
     return a;
 }
 
+// n_fix: fix-up slots the split kernel wrote (its grid for the balanced
+// tensor-core kernel, 0 for the item-per-CTA kernel)
+// The combine is a programmatic dependent launch: its CTAs may be scheduled
+// while the split kernel's last CTAs finish (hiding the launch latency) and
+// wait in griddepcontrol.wait for that grid to complete.
+// n_fix: fix-up slots the split kernel wrote (its grid for the balanced
+// tensor-core kernel, 0 for the item-per-CTA kernel)
 template <int D>
-attn_status launch_combine(const DecodeLaunch& L, const DecodePlan& plan, const DecArgs& a) {
+attn_status launch_combine(const DecodeLaunch& L, const DecodePlan& plan, const DecArgs& a, int n_fix) {
     const int nwarps = L.B * L.Hq;
-    decode_combine_kernel<D><<<(nwarps + 3) / 4, 128, 0, L.stream>>>(
-        L.kv_len, a.ws_prefix, a.ws_lse, a.ws_o, static_cast<__half*>(L.out), L.lse, L.B, L.Hq, a.G, plan.GH,
-        plan.HG, plan.split, a.cap_eff, L.window);
-    const cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((nwarps + 3) / 4);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, L.kv_len, (const int32_t*)a.ws_prefix,
+                                       (const float*)a.ws_lse, (const float*)a.ws_o, static_cast<__half*>(L.out), L.lse,
+                                       L.B, L.Hq, a.G, plan.GH, plan.HG, plan.split, a.cap_eff, L.window,
+                                       (const int32_t*)a.ws_fix_meta, (const float*)a.ws_fix_lse,
+                                       (const float*)a.ws_fix_o, n_fix, plan.n_hb);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode combine launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }
@@ -739,11 +866,12 @@ attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan) {
         attr_set[dev] = true;
     }
     const DecArgs a = make_dec_args(L, plan, 16);
-    tcdec::decode_tc_kernel<D, NH><<<decode_grid(plan), tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a,
-                                                                                                    q_rows);
+    // balanced: every CTA takes an equal share of the tiles (see decode_tc.cuh)
+    const int grid = sm_count() < plan.n_fix ? sm_count() : plan.n_fix;
+    tcdec::decode_tc_kernel<D, NH><<<grid, tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a, q_rows);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode tc launch failed: %s", cudaGetErrorString(e));
-    return launch_combine<D>(L, plan, a);
+    return launch_combine<D>(L, plan, a, grid);
 }
 
 template <int D, bool I8, int GH>
@@ -754,10 +882,11 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
     const bool paged = L.page_table != nullptr;
     if constexpr (!I8 && D != 256) {
         // both contractions on the tensor cores where the boxes allow it:
-        // 16-row boxes must not cross a page, and cover at most Hkv heads
+        // 16-row boxes must not cross a page, and cover at most Hkv heads;
+        // batches of up to 2048 sequences
         int nh = 1;
         while (nh < plan.nh_box) nh <<= 1;
-        if ((!paged || L.page_size % 16 == 0) && nh <= L.Hkv) {
+        if ((!paged || L.page_size % 16 == 0) && nh <= L.Hkv && L.B <= tcdec::kMaxBatch) {
             switch (nh) {
                 case 1: return launch_decode_tc<D, 1>(L, plan);
                 case 2: return launch_decode_tc<D, 2>(L, plan);
@@ -813,7 +942,7 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
     decode_split_kernel<D, I8, GH><<<decode_grid(plan), kDecThreads, C::SMEM_ALLOC, L.stream>>>(tk, tv, tks, tvs, a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode split launch failed: %s", cudaGetErrorString(e));
-    return launch_combine<D>(L, plan, a);
+    return launch_combine<D>(L, plan, a, 0);
 }
 
 template <int D, bool I8>
@@ -855,12 +984,24 @@ bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys,
     plan->split = split;
     // +1 split: aligning a window start down to the tile can add one partial split
     plan->max_items = units * ((max_kv + split - 1) / split + 1);
+    // fix-up slots: the balanced kernel launches at most this many CTAs
+    plan->n_fix = plan->max_items < kDecodeMaxFix ? (int)plan->max_items : kDecodeMaxFix;
     const size_t rows = (size_t)plan->max_items * NW * plan->GH;   // (item, warp, head) partial rows
-    size_t off = ((size_t)(B + 1) * 4 + 255) / 256 * 256;
+    const size_t frows = (size_t)plan->n_fix * NW * plan->GH;      // (CTA, warp, head) fix-up rows
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    size_t off = up((size_t)(B + 1) * 4);                          // item prefix
+    plan->off_tpref = off;
+    off += up((size_t)(B + 1) * 4);
+    plan->off_fix_meta = off;
+    off += up((size_t)plan->n_fix * 4);
     plan->off_lse = off;
-    off += (rows * 4 + 255) / 256 * 256;
+    off += up(rows * 4);
+    plan->off_fix_lse = off;
+    off += up(frows * 4);
     plan->off_o = off;
-    off += rows * D * 4;
+    off += up(rows * D * 4);
+    plan->off_fix_o = off;
+    off += frows * D * 4;
     plan->bytes = off;
     return true;
 }

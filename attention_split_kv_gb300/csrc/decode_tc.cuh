@@ -38,6 +38,7 @@ namespace tcdec {
 constexpr int kThreads = 96;
 constexpr int TR = 128;                       // rows of the K/V operand per MMA tile
 constexpr int QROWS = 32;                     // query rows written (NW units x up to 4 heads)
+constexpr int kMaxBatch = 2048;               // sequences per call (two prefixes live in shared memory)
 
 template <int D>
 struct Cfg {
@@ -61,7 +62,8 @@ struct Cfg {
     // s_full, s_free, p_full[2], pv_done[2], o_free[2], teardown
     static constexpr int N_BARS = 2 * NK + 2 * NV + 15;
     static constexpr uint32_t OFF_PREFIX = OFF_BARS + N_BARS * 8;
-    static constexpr uint32_t PREFIX_BYTES = ((kDecodeMaxBatch + 1) * 4 + 127) / 128 * 128;
+    static constexpr uint32_t PREFIX_ONE = ((kMaxBatch + 1) * 4 + 127) / 128 * 128;
+    static constexpr uint32_t PREFIX_BYTES = 2 * PREFIX_ONE;        // item prefix, tile prefix
     static constexpr uint32_t OFF_MISC = OFF_PREFIX + PREFIX_BYTES;   // scan scratch, abort flag, TMEM base
     static constexpr uint32_t SMEM_USED = OFF_MISC + 256;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
@@ -92,41 +94,66 @@ __device__ __forceinline__ float pick(const uint32_t* c, int sel) {
     }
 }
 
-// The CTA's tiles in issue order: work items it = blockIdx.x, +gridDim.x, ...,
-// each cut into MMA tiles of NBX 16-token groups.
-struct Cursor {
-    int it, idx, mt, n_mt;   // item, its index within this CTA, MMA tile within it, tiles in it
-    Item I;
+// Work split.  The MMA tiles of a launch are numbered sequence by sequence,
+// head block by head block: (b, hb) has Tb tiles of TT tokens from the first
+// kept key rounded down to 16.  CTA c takes tiles [c*NT/G, (c+1)*NT/G) of the
+// NT in total, so every CTA streams the same amount of cache whatever the
+// sequence lengths.  Consecutive tiles of one (b, hb) form a run with one
+// online softmax.  A run that starts where a split of the item enumeration
+// starts writes its partial into that item's row and -inf lse into the rows
+// of the items that start inside it; only a CTA's first run can start inside
+// an item, and it writes a fix-up slot of its own, tagged with (b, hb), which
+// the combine pass merges with the item rows.
+struct TileCur {
+    int x, x_end;          // current tile, end of this CTA's range
+    int b, hb, t, Tb;      // sequence, head block, tile within (b, hb), tiles per (b, hb)
+    int a, start, end;     // first token of tile 0 (16-aligned), kept keys [start, end)
+    int run;               // index of the current run within this CTA
+    bool first, last;      // first / last tile of its run
 };
 
-template <int NBX>
-__device__ __forceinline__ void cursor_load(Cursor& c, int total, const int* pref, const DecArgs& A) {
-    c.mt = 0;
-    c.n_mt = 0;
-    if (c.it < total) {
-        c.I = decode_item<16>(c.it, pref, A);
-        c.n_mt = (c.I.ntile + NBX - 1) / NBX;
+template <int TT>
+__device__ __forceinline__ void tcur_locate(TileCur& c, const int* tpref, const DecArgs& A) {
+    int lo = 0, hi = A.B;   // largest b with tpref[b] <= x: a sequence with tiles
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tpref[mid] <= c.x) lo = mid; else hi = mid;
+    }
+    c.b = lo;
+    seq_range(__ldg(&A.kv_len[lo]), A.cap_eff, A.window, c.start, c.end);
+    c.a = (c.start / 16) * 16;
+    c.Tb = (tpref[lo + 1] - tpref[lo]) / A.n_hb;
+    const int rel = c.x - tpref[lo];
+    c.hb = rel / c.Tb;
+    c.t = rel - c.hb * c.Tb;
+}
+template <int TT>
+__device__ __forceinline__ void tcur_mark_last(TileCur& c) {
+    c.last = (c.t + 1 == c.Tb) || (c.x + 1 == c.x_end);
+}
+template <int TT>
+__device__ __forceinline__ void tcur_start(TileCur& c, const int* tpref, const DecArgs& A) {
+    const long long nt = tpref[A.B];
+    c.x = (int)((long long)blockIdx.x * nt / gridDim.x);
+    c.x_end = (int)((long long)(blockIdx.x + 1) * nt / gridDim.x);
+    c.run = 0;
+    c.first = true;
+    if (c.x < c.x_end) {
+        tcur_locate<TT>(c, tpref, A);
+        tcur_mark_last<TT>(c);
     }
 }
-template <int NBX>
-__device__ __forceinline__ void cursor_start(Cursor& c, int total, const int* pref, const DecArgs& A) {
-    c.it = blockIdx.x;
-    c.idx = 0;
-    cursor_load<NBX>(c, total, pref, A);
-    while (c.it < total && c.n_mt == 0) {   // items without tiles hold no keys
-        c.it += gridDim.x;
-        ++c.idx;
-        cursor_load<NBX>(c, total, pref, A);
+template <int TT>
+__device__ __forceinline__ void tcur_next(TileCur& c, const int* tpref, const DecArgs& A) {
+    if (++c.x >= c.x_end) return;
+    c.first = false;
+    if (++c.t == c.Tb) {
+        ++c.run;
+        c.first = true;
+        c.t = 0;
+        if (++c.hb == A.n_hb) tcur_locate<TT>(c, tpref, A);
     }
-}
-template <int NBX>
-__device__ __forceinline__ void cursor_next(Cursor& c, int total, const int* pref, const DecArgs& A) {
-    if (++c.mt < c.n_mt) return;
-    do {
-        c.it += gridDim.x;
-        ++c.idx;
-        cursor_load<NBX>(c, total, pref, A);
-    } while (c.it < total && c.n_mt == 0);
+    tcur_mark_last<TT>(c);
 }
 
 template <int D, int NH>
@@ -142,7 +169,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
-    int* pref = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
+    int* pref = reinterpret_cast<int*>(smem + C::OFF_PREFIX);     // item prefix over sequences
+    int* tpref = reinterpret_cast<int*>(smem + C::OFF_PREFIX + C::PREFIX_ONE);   // tile prefix over sequences
     int* scratch = reinterpret_cast<int*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 128);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 132);
@@ -180,9 +208,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     tc_fence_before();
     build_prefix(A, pref, scratch);   // ends with __syncthreads
+    build_prefix_of(A, tpref, scratch, [&](int start, int end) {
+        return end > start ? A.n_hb * ((end - (start / 16) * 16 + TT - 1) / TT) : 0;
+    });
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const int total = pref[A.B];
     if (blockIdx.x == 0) {
         for (int b = threadIdx.x; b <= A.B; b += blockDim.x) A.ws_prefix[b] = pref[b];
     }
@@ -191,7 +221,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (warp == 1) {
         // ------------------------------------------------------------ TMA producers
-        // lane 0 loads Q' (once per item) and the K tiles, lane 1 the V tiles;
+        // lane 0 loads Q' (once per run) and the K tiles, lane 1 the V tiles;
         // each waits only for its own buffers
         if (lane < 2) {
             const bool is_k = lane == 0;
@@ -201,26 +231,26 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t ring = sbase + (is_k ? C::OFF_RING : C::OFF_VRING);
             tma_prefetch_desc(tm);
             if (is_k) tma_prefetch_desc(&tm_q);
-            Cursor c;
-            cursor_start<NBX>(c, total, pref, A);
+            TileCur c;
+            tcur_start<TT>(c, tpref, A);
             uint32_t j = 0;
-            int q_last[2] = {-1, -1};   // last item whose Q' was loaded into each buffer
+            int q_last[2] = {-1, -1};   // last run whose Q' was loaded into each buffer
             bool ok = true;
-            for (; c.it < total; cursor_next<NBX>(c, total, pref, A), ++j) {
-                if (is_k && c.mt == 0) {
-                    // Q' of this item: query heads hb*QB .. +q_rows of sequence b
-                    const int qb = c.idx & 1;
-                    if (c.idx >= 2 &&
-                        !mbar_wait(bar(B_QEMPTY + qb), ((c.idx >> 1) - 1) & 1, abort_flag, A.err, kErrTimeoutSlot)) {
+            for (; c.x < c.x_end; tcur_next<TT>(c, tpref, A), ++j) {
+                if (is_k && c.first) {
+                    // Q' of this run: query heads hb*QB .. +q_rows of sequence b
+                    const int qb = c.run & 1;
+                    if (c.run >= 2 &&
+                        !mbar_wait(bar(B_QEMPTY + qb), ((c.run >> 1) - 1) & 1, abort_flag, A.err, kErrTimeoutSlot)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(bar(B_QFULL + qb), NCH * q_rows * 128);
-                    q_last[qb] = c.idx;
+                    q_last[qb] = c.run;
 #pragma unroll
                     for (int ch = 0; ch < NCH; ++ch)
                         tma_load_3d(sbase + C::OFF_Q + qb * C::QBUF + ch * C::QCH, &tm_q, bar(B_QFULL + qb), ch * 64,
-                                    c.I.hb * QB, c.I.b);
+                                    c.hb * QB, c.b);
                 }
                 const int slot = j % NS;
                 if (j >= (uint32_t)NS &&
@@ -228,20 +258,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     ok = false;
                     break;
                 }
-                const int g0 = (c.I.hb * NW) / A.HG;
-                const int nbox = min(NBX, c.I.ntile - c.mt * NBX);
+                const int g0 = (c.hb * NW) / A.HG;
+                const int t0 = c.a + c.t * TT;
+                const int nbox = min(NBX, (c.end - t0 + 15) / 16);
                 mbar_arrive_expect_tx(bar(b_full + slot), nbox * NCH * BOXB);
                 for (int bx = 0; bx < nbox; ++bx) {
-                    const int t0 = c.I.ks + (c.mt * NBX + bx) * 16;
-                    int page = c.I.b, row = t0;
+                    const int tk = t0 + bx * 16;
+                    int page = c.b, row = tk;
                     if (A.paged) {
-                        page = __ldg(&A.page_table[(size_t)c.I.b * A.max_pages + t0 / A.P]);
+                        page = __ldg(&A.page_table[(size_t)c.b * A.max_pages + tk / A.P]);
                         if (page < 0 || page >= A.n_pages) {
                             // a page id outside the pool: read page 0 instead and report it
                             atomicExch(A.err, kErrBadPage);
                             page = 0;
                         }
-                        row = t0 % A.P;
+                        row = tk % A.P;
                     }
 #pragma unroll
                     for (int ch = 0; ch < NCH; ++ch)
@@ -264,22 +295,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16_f32(128, TR, false);
             constexpr uint32_t idesc_o = idesc_f16_f32(128, D, true);
-            Cursor cs, cp;                    // next S to issue, next PV to issue
-            cursor_start<NBX>(cs, total, pref, A);
-            cursor_start<NBX>(cp, total, pref, A);
+            TileCur cs, cp;                   // next S to issue, next PV to issue
+            tcur_start<TT>(cs, tpref, A);
+            tcur_start<TT>(cp, tpref, A);
             uint32_t js = 0;                  // tiles whose S has been issued
             bool ok = true;
-            // S_js: Q' of its item (buffer idx & 1) times the K tile of ring slot js
+            // S_js: Q' of its run (buffer run & 1) times the K tile of ring slot js
             auto issue_s = [&]() -> bool {
                 const int slot = js % NK;
-                if (cs.mt == 0 &&
-                    !mbar_wait(bar(B_QFULL + (cs.idx & 1)), (cs.idx >> 1) & 1, abort_flag, A.err, kErrTimeoutLoad))
+                if (cs.first &&
+                    !mbar_wait(bar(B_QFULL + (cs.run & 1)), (cs.run >> 1) & 1, abort_flag, A.err, kErrTimeoutLoad))
                     return false;
                 // the single S buffer: the softmax has tile js-1 in registers
                 if (js > 0 && !mbar_wait(bar(B_SFREE), (js - 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax)) return false;
                 if (!mbar_wait(bar(B_KFULL + slot), (js / NK) & 1, abort_flag, A.err, kErrTimeoutLoad)) return false;
                 tc_fence_after();
-                const uint32_t qb = sbase + C::OFF_Q + (cs.idx & 1) * C::QBUF;
+                const uint32_t qb = sbase + C::OFF_Q + (cs.run & 1) * C::QBUF;
                 const uint32_t kb = sbase + C::OFF_RING + slot * C::KV_BYTES;
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch)
@@ -291,22 +322,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 tc_commit(bar(B_SFULL));
                 tc_commit(bar(B_KEMPTY + slot));
-                if (cs.mt + 1 == cs.n_mt) tc_commit(bar(B_QEMPTY + (cs.idx & 1)));   // last S of the item
+                if (cs.last) tc_commit(bar(B_QEMPTY + (cs.run & 1)));   // last S of the run
                 ++js;
-                cursor_next<NBX>(cs, total, pref, A);
+                tcur_next<TT>(cs, tpref, A);
                 return true;
             };
-            if (cs.it < total) ok = issue_s();
-            for (uint32_t j = 0; ok && cp.it < total; ++j, cursor_next<NBX>(cp, total, pref, A)) {
+            if (cs.x < cs.x_end) ok = issue_s();
+            for (uint32_t j = 0; ok && cp.x < cp.x_end; ++j, tcur_next<TT>(cp, tpref, A)) {
                 // S_{j+1} first (it waits for the softmax to hold S_j), so QK^T of
                 // the next tile overlaps the exponentials of this one
-                if (cs.it < total && !(ok = issue_s())) break;
+                if (cs.x < cs.x_end && !(ok = issue_s())) break;
                 if (!mbar_wait(bar(B_PFULL + (j & 1)), (j >> 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax)) break;
-                const int ob = cp.idx & 1;
-                // the first PV of an item overwrites its O buffer: the epilogue of the
-                // item that used it before must have read it
-                if (cp.mt == 0 && cp.idx >= 2 &&
-                    !mbar_wait(bar(B_OFREE + ob), ((cp.idx >> 1) - 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax))
+                const int ob = cp.run & 1;
+                // the first PV of a run overwrites its O buffer: the epilogue of the
+                // run that used it before must have read it
+                if (cp.first && cp.run >= 2 &&
+                    !mbar_wait(bar(B_OFREE + ob), ((cp.run >> 1) - 1) & 1, abort_flag, A.err, kErrTimeoutSoftmax))
                     break;
                 const int slot = j % NV;
                 if (!mbar_wait(bar(B_VFULL + slot), (j / NV) & 1, abort_flag, A.err, kErrTimeoutLoad)) break;
@@ -317,7 +348,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int kk = 0; kk < TR / 16; ++kk) {
                     // 16 rows per MMA: 8 TMEM columns of P, 16 rows of V (2048 bytes)
                     const uint64_t b = smem_desc_sw128(vb + kk * 16 * 128, C::CHUNK, 1024);
-                    tc_mma_f16_ts(tmem + C::COL_O + ob * D, p_tmem + kk * 8, b, idesc_o, (cp.mt > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_f16_ts(tmem + C::COL_O + ob * D, p_tmem + kk * 8, b, idesc_o, (!cp.first || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(B_PVDONE + (j & 1)));
                 tc_commit(bar(B_VEMPTY + slot));
@@ -333,10 +364,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int wu = r / GH, hs = r - wu * GH;    // unit of the head block, head inside it
         const uint32_t lane_base = tmem;            // warp 0: TMEM lanes 0-31
 
-        // the split epilogue, run one tile late: (lse, o / l) of this thread's query head
+        TileCur c;
+        tcur_start<TT>(c, tpref, A);
+        // the fix-up tag of this CTA: (b, hb) if its first run starts inside a split
+        if (lane == 0) {
+            int tag = -1;
+            if (c.x < c.x_end && (c.t * TT) % A.split != 0) tag = c.b * A.n_hb + c.hb;
+            A.ws_fix_meta[blockIdx.x] = tag;
+        }
+
+        // a run's epilogue, run one tile late: (lse, o / l) of this thread's query
+        // head into the item row (or the fix-up slot), -inf into the rows of the
+        // items that start inside the run
         struct Pending {
             bool on, act;
-            int it, ob;
+            int b, hb, t_first, t_last, ob, ns;
             uint32_t j_last;
             float m, l;
         } pend;
@@ -346,154 +388,177 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 return false;
             tc_fence_after();
             const float inv = pend.l > 0.f ? 1.0f / pend.l : 0.f;
-            const size_t prow = ((size_t)pend.it * NW + wu) * GH + hs;
+            const int f = pend.t_first * TT;          // first token of the run, from the sequence's tile 0
+            const int item0 = pref[pend.b] + pend.hb * pend.ns;
+            float* o_dst;
+            float* l_dst;
+            if (f % A.split == 0) {
+                const size_t prow = ((size_t)(item0 + f / A.split) * NW + wu) * GH + hs;
+                o_dst = A.ws_o + prow * D;
+                l_dst = A.ws_lse + prow;
+            } else {
+                const size_t prow = ((size_t)blockIdx.x * NW + wu) * GH + hs;
+                o_dst = A.ws_fix_o + prow * D;
+                l_dst = A.ws_fix_lse + prow;
+            }
 #pragma unroll 1
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
                 tc_ld_32x32b_x32(lane_base + C::COL_O + pend.ob * D + q * 32, o);
                 tc_wait_ld();
                 if (pend.act) {
-                    float4* dst = reinterpret_cast<float4*>(A.ws_o + prow * D + q * 32);
+                    float4* dst = reinterpret_cast<float4*>(o_dst + q * 32);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                                              __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
                 }
             }
-            if (pend.act) A.ws_lse[prow] = pend.l > 0.f ? pend.m + __log2f(pend.l) : -INFINITY;
+            if (pend.act) {
+                *l_dst = pend.l > 0.f ? pend.m + __log2f(pend.l) : -INFINITY;
+                const int s_hi = min(((pend.t_last + 1) * TT - 1) / A.split, pend.ns - 1);
+                for (int sp = f / A.split + 1; sp <= s_hi; ++sp)
+                    A.ws_lse[((size_t)(item0 + sp) * NW + wu) * GH + hs] = -INFINITY;
+            }
             tc_fence_before();
             mbar_arrive(bar(B_OFREE + pend.ob));
             pend.on = false;
             return true;
         };
 
-        Cursor c;
-        cursor_start<NBX>(c, total, pref, A);
         uint32_t j = 0;
         bool ok = true;
-        while (ok && c.it < total) {
-            const Cursor item = c;
-            const int u = item.I.hb * NW + wu;
-            const bool act = wu < NW && r < QB && u < A.U;
-            const int g = act ? u / A.HG : 0;
-            const int gl = act ? g - (item.I.hb * NW) / A.HG : 0;   // kv head inside the tile (row % NH)
-            const int ob = item.idx & 1;
-            float m_used = -INFINITY, l_sum = 0.f;
-            for (int mt = 0; mt < item.n_mt; ++mt, ++j) {
-                if (!mbar_wait(bar(B_SFULL), j & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
-                tc_fence_after();
-                float s[TT];
-                {
-                    uint32_t v[TR];
+        bool act = false;
+        int gl = 0, t_first = 0;
+        float m_used = -INFINITY, l_sum = 0.f;
+        for (; c.x < c.x_end; tcur_next<TT>(c, tpref, A), ++j) {
+            if (c.first) {
+                const int u = c.hb * NW + wu;
+                act = wu < NW && r < QB && u < A.U;
+                gl = act ? u / A.HG - (c.hb * NW) / A.HG : 0;   // kv head inside the tile (row % NH)
+                t_first = c.t;
+                m_used = -INFINITY;
+                l_sum = 0.f;
+            }
+            const int ob = c.run & 1;
+            if (!mbar_wait(bar(B_SFULL), j & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
+            tc_fence_after();
+            float s[TT];
+            {
+                uint32_t v[TR];
 #pragma unroll
-                    for (int q = 0; q < TR / 32; ++q)
-                        tc_ld_32x32b_x32(lane_base + C::COL_S + q * 32, *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
-                    tc_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(bar(B_SFREE));         // S is in registers: the next QK^T may run
+                for (int q = 0; q < TR / 32; ++q)
+                    tc_ld_32x32b_x32(lane_base + C::COL_S + q * 32, *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
+                tc_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(B_SFREE));         // S is in registers: the next QK^T may run
 #pragma unroll
-                    for (int t = 0; t < TT; ++t) s[t] = pick<NH>(v + t * NH, gl);
+                for (int t = 0; t < TT; ++t) s[t] = pick<NH>(v + t * NH, gl);
+            }
+            const int t0 = c.a + c.t * TT;
+            const int v_lo = max(c.start - t0, 0);
+            const int v_hi = min(c.end - t0, TT);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+                float x = s[t] * A.qscale;
+                if (A.cap_log2 > 0.f) x = A.cap_log2 * tanh_abs_accurate(x);
+                x = (act && t >= v_lo && t < v_hi) ? x : -INFINITY;
+                s[t] = x;
+                mx = fmaxf(mx, x);
+            }
+            const bool need = mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx > -INFINITY);
+            const bool rescale = __any_sync(0xffffffffu, need) && !c.first;
+            float alpha = 1.f;
+            if (need) {
+                const float m_new = fmaxf(mx, m_used);
+                alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
+                l_sum *= alpha;
+                m_used = m_new;
+            }
+            const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
+            uint32_t pw[64];                    // the P row: 128 f16 entries
+            float ls = 0.f;
+            if constexpr (NH == 1) {
+#pragma unroll
+                for (int t = 0; t < TT; t += 2) {
+                    const float p0 = ex2_approx(s[t] - m_off), p1 = ex2_approx(s[t + 1] - m_off);
+                    ls += p0 + p1;
+                    const __half2 h2 = __floats2half2_rn(p0, p1);
+                    pw[t / 2] = act ? *reinterpret_cast<const uint32_t*>(&h2) : 0u;
                 }
-                const int t0 = item.I.ks + mt * TT;
-                const int v_lo = max(item.I.start - t0, 0);
-                const int v_hi = min(item.I.ke - t0, TT);
-                float mx = -INFINITY;
+            } else {
+                const int hp = gl >> 1;
 #pragma unroll
                 for (int t = 0; t < TT; ++t) {
-                    float x = s[t] * A.qscale;
-                    if (A.cap_log2 > 0.f) x = A.cap_log2 * tanh_abs_accurate(x);
-                    x = (act && t >= v_lo && t < v_hi) ? x : -INFINITY;
-                    s[t] = x;
-                    mx = fmaxf(mx, x);
-                }
-                const bool need = mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx > -INFINITY);
-                const bool rescale = __any_sync(0xffffffffu, need) && mt > 0;
-                float alpha = 1.f;
-                if (need) {
-                    const float m_new = fmaxf(mx, m_used);
-                    alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
-                    l_sum *= alpha;
-                    m_used = m_new;
-                }
-                const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
-                uint32_t pw[64];                    // the P row: 128 f16 entries
-                float ls = 0.f;
-                if constexpr (NH == 1) {
+                    const float p = ex2_approx(s[t] - m_off);
+                    ls += p;
+                    const uint32_t h = __half_as_ushort(__float2half_rn(p));
+                    const uint32_t word = act ? ((gl & 1) ? (h << 16) : h) : 0u;
 #pragma unroll
-                    for (int t = 0; t < TT; t += 2) {
-                        const float p0 = ex2_approx(s[t] - m_off), p1 = ex2_approx(s[t + 1] - m_off);
-                        ls += p0 + p1;
-                        const __half2 h2 = __floats2half2_rn(p0, p1);
-                        pw[t / 2] = act ? *reinterpret_cast<const uint32_t*>(&h2) : 0u;
-                    }
-                } else {
-                    const int hp = gl >> 1;
-#pragma unroll
-                    for (int t = 0; t < TT; ++t) {
-                        const float p = ex2_approx(s[t] - m_off);
-                        ls += p;
-                        const uint32_t h = __half_as_ushort(__float2half_rn(p));
-                        const uint32_t word = act ? ((gl & 1) ? (h << 16) : h) : 0u;
-#pragma unroll
-                        for (int w = 0; w < NH / 2; ++w) pw[t * (NH / 2) + w] = (w == hp) ? word : 0u;
-                    }
+                    for (int w = 0; w < NH / 2; ++w) pw[t * (NH / 2) + w] = (w == hp) ? word : 0u;
                 }
-                l_sum += ls;
-                if (rescale) {
-                    // O must not be in flight while it is rescaled
-                    if (!mbar_wait(bar(B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int q = 0; q < D / 32; ++q) {
-                        uint32_t o[32];
-                        tc_ld_32x32b_x32(lane_base + C::COL_O + ob * D + q * 32, o);
-                        tc_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tc_st_32x32b_x32(lane_base + C::COL_O + ob * D + q * 32, o);
-                    }
-                }
-                // P buffer j & 1 was last read by PV_{j-2}
-                if (j >= 2 && !mbar_wait(bar(B_PVDONE + (j & 1)), ((j - 2) >> 1) & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
-                tc_st_32x32b_x32(lane_base + C::COL_P + (j & 1) * 64, *reinterpret_cast<const uint32_t(*)[32]>(pw));
-                tc_st_32x32b_x32(lane_base + C::COL_P + (j & 1) * 64 + 32, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32));
-                if (v_lo > 0 || v_hi < TT) {
-                    // zero the V rows of masked tokens (all NH heads, every chunk), once
-                    // the tile's copy has landed
-                    if (!mbar_wait(bar(B_VFULL + (j % NV)), (j / NV) & 1, abort_flag, A.err, kErrTimeoutLoad)) { ok = false; break; }
-                    uint8_t* vt = smem + C::OFF_VRING + (j % NV) * C::KV_BYTES;
-                    const int lo_end = v_lo * NH * 128, hi_beg = v_hi * NH * 128;
-#pragma unroll 1
-                    for (int ch = 0; ch < NCH; ++ch) {
-                        uint8_t* cb = vt + ch * C::CHUNK;
-                        for (int o = lane * 16; o < lo_end; o += 32 * 16) *reinterpret_cast<uint4*>(cb + o) = make_uint4(0u, 0u, 0u, 0u);
-                        for (int o = hi_beg + lane * 16; o < (int)C::CHUNK; o += 32 * 16)
-                            *reinterpret_cast<uint4*>(cb + o) = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
-                }
-                tc_wait_st();
-                tc_fence_before();
-                mbar_arrive(bar(B_PFULL + (j & 1)));
-                // the previous item's epilogue, now that this item's first P is out
-                if (pend.on && !epilogue()) { ok = false; break; }
             }
-            if (!ok) break;
-            pend.on = true;
-            pend.act = act;
-            pend.it = item.it;
-            pend.ob = ob;
-            pend.j_last = j - 1;
-            pend.m = m_used;
-            pend.l = l_sum;
-            c = item;
-            c.mt = c.n_mt - 1;
-            cursor_next<NBX>(c, total, pref, A);
+            l_sum += ls;
+            if (rescale) {
+                // O must not be in flight while it is rescaled
+                if (!mbar_wait(bar(B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    tc_ld_32x32b_x32(lane_base + C::COL_O + ob * D + q * 32, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tc_st_32x32b_x32(lane_base + C::COL_O + ob * D + q * 32, o);
+                }
+            }
+            // P buffer j & 1 was last read by PV_{j-2}
+            if (j >= 2 && !mbar_wait(bar(B_PVDONE + (j & 1)), ((j - 2) >> 1) & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }
+            tc_st_32x32b_x32(lane_base + C::COL_P + (j & 1) * 64, *reinterpret_cast<const uint32_t(*)[32]>(pw));
+            tc_st_32x32b_x32(lane_base + C::COL_P + (j & 1) * 64 + 32, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32));
+            if (v_lo > 0 || v_hi < TT) {
+                // zero the V rows of masked tokens (all NH heads, every chunk), once
+                // the tile's copy has landed
+                if (!mbar_wait(bar(B_VFULL + (j % NV)), (j / NV) & 1, abort_flag, A.err, kErrTimeoutLoad)) { ok = false; break; }
+                uint8_t* vt = smem + C::OFF_VRING + (j % NV) * C::KV_BYTES;
+                const int lo_end = v_lo * NH * 128, hi_beg = v_hi * NH * 128;
+#pragma unroll 1
+                for (int ch = 0; ch < NCH; ++ch) {
+                    uint8_t* cb = vt + ch * C::CHUNK;
+                    for (int o = lane * 16; o < lo_end; o += 32 * 16) *reinterpret_cast<uint4*>(cb + o) = make_uint4(0u, 0u, 0u, 0u);
+                    for (int o = hi_beg + lane * 16; o < (int)C::CHUNK; o += 32 * 16)
+                        *reinterpret_cast<uint4*>(cb + o) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(B_PFULL + (j & 1)));
+            // the previous run's epilogue, now that this run's first P is out
+            if (pend.on && !epilogue()) { ok = false; break; }
+            if (c.last) {
+                pend.on = true;
+                pend.act = act;
+                pend.b = c.b;
+                pend.hb = c.hb;
+                pend.t_first = t_first;
+                pend.t_last = c.t;
+                pend.ob = ob;
+                pend.ns = seq_splits(c.start, c.end, A.split);
+                pend.j_last = j;
+                pend.m = m_used;
+                pend.l = l_sum;
+            }
         }
         if (ok && pend.on) epilogue();
     }
     tc_fence_before();
     __syncthreads();
+    // this CTA's partials are written: the combine pass may be scheduled (it
+    // still waits for the whole grid to finish)
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
