@@ -57,6 +57,9 @@ def _load():
             lib.oracle_prefill.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, f64, f64,
                                            i32, P, P, P, P, i32]
             lib.oracle_prefill.restype = i32
+            lib.oracle_prefill_paged.argtypes = [P, P, P, P, P, P, i32, i32, i64, i32, i32, i32, i32,
+                                                 i32, f64, f64, i32, P, P, P, P, i32]
+            lib.oracle_prefill_paged.restype = i32
             lib.oracle_max_threads.restype = i32
             _lib = lib
     return _lib
@@ -152,4 +155,35 @@ def prefill(case, rows=None, n_threads: int = 0):
                             n_rows, _ptr(ri), _ptr(rh), _ptr(out), _ptr(lse), int(n_threads))
     if rc != 0:
         raise ValueError("oracle_prefill rejected its arguments")
+    return out, lse
+
+
+def prefill_paged(case, rows=None, n_threads: int = 0):
+    """Oracle chunked prefill / multi-token decode for a ChunkCase-like object.
+
+    rows: None for every (packed query row, head) in row-major order, or a list
+    of (row, head) pairs.  Returns (out float64 [n, D], lse float64 [n]).
+    """
+    lib = _load()
+    q, k, v = _f16_bits(case.q), _f16_bits(case.k), _f16_bits(case.v)
+    q_start = _np(case.q_start).astype(np.int32, copy=False)
+    kv_len = _np(case.kv_len).astype(np.int32, copy=False)
+    pt = _np(case.page_table).astype(np.int32, copy=False)
+    total_q = int(q_start[-1])
+    if rows is None:
+        n_rows, rr, rh = -1, None, None
+        n = total_q * case.n_heads
+    else:
+        rows = np.asarray(rows, dtype=np.int32).reshape(-1, 2)
+        n_rows = n = rows.shape[0]
+        rr, rh = np.ascontiguousarray(rows[:, 0]), np.ascontiguousarray(rows[:, 1])
+    out = np.zeros((n, case.head_dim), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    rc = lib.oracle_prefill_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(q_start), _ptr(kv_len), _ptr(pt),
+                                  int(case.page_size), int(case.max_pages), int(case.k.shape[0]),
+                                  case.batch, case.n_heads, case.n_kv_heads, case.head_dim,
+                                  int(case.window), float(case.softcap), float(case.scale),
+                                  n_rows, _ptr(rr), _ptr(rh), _ptr(out), _ptr(lse), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_prefill_paged rejected its arguments")
     return out, lse

@@ -234,6 +234,69 @@ int oracle_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     return 0;
 }
 
+/*
+ * Chunked prefill / multi-token decode against a paged cache: sequence b has
+ * q_len = q_start[b+1] - q_start[b] new query tokens, packed as rows
+ * q_start[b] .. q_start[b+1]-1 of q [total_q][Hq][D].  Their K/V are already
+ * the last q_len of the kv_len[b] cache tokens, so query i sits at position
+ * kv_len[b] - q_len + i and attends causally (doppler attention.js,
+ * createAttentionUniformBuffer: seqLen new tokens at startPos over kvLen keys,
+ * causal, with the paged layout's page table and pageSize; decode is the
+ * seqLen = 1 case).  Keys past the cache capacity max_pages*P do not exist; a
+ * query whose position is negative sees no key.
+ * rows: n_rows (packed query row, head) pairs, or n_rows < 0 for all
+ * total_q*Hq in (row, head) row-major order.  out: [n][D], lse: [n].
+ */
+int oracle_prefill_paged(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const int32_t* q_start, const int32_t* kv_len, const int32_t* page_table,
+                         int page_size, int max_pages, long n_pages,
+                         int B, int Hq, int Hkv, int D, int window, double softcap, double scale,
+                         int n_rows, const int32_t* rows_r, const int32_t* rows_h,
+                         double* out, double* lse, int n_threads)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0 || page_size <= 0) return -1;
+    int G = Hq / Hkv;
+    long total_q = q_start[B];
+    long cap = (long)max_pages * page_size;
+    long n = n_rows < 0 ? total_q * Hq : n_rows;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 4)
+#endif
+    for (long r = 0; r < n; ++r) {
+        long row = n_rows < 0 ? r / Hq : rows_r[r];
+        int h = n_rows < 0 ? (int)(r % Hq) : rows_h[r];
+        int b = 0;
+        while (b + 1 < B && q_start[b + 1] <= row) ++b;      /* the sequence owning the row */
+        long q_len = q_start[b + 1] - q_start[b];
+        long i = row - q_start[b];
+        long L = kv_len[b] < cap ? kv_len[b] : cap;
+        if (L < 0) L = 0;
+        long pos = (long)kv_len[b] - q_len + i;
+        int g = h / G;
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);
+        for (int d = 0; d < D; ++d)
+            qd[d] = oracle_f16_to_double(q[(row * Hq + h) * (long)D + d]);
+        for (long t = 0; t < L; ++t)
+            for (int d = 0; d < D; ++d) {
+                Kd[t * D + d] = oracle_cache_value(k, NULL, 0, page_table, page_size, max_pages, cap,
+                                                   n_pages, b, t, g, d, Hkv, D);
+                Vd[t * D + d] = oracle_cache_value(v, NULL, 0, page_table, page_size, max_pages, cap,
+                                                   n_pages, b, t, g, d, Hkv, D);
+            }
+        if (pos < 0) {                     /* no key at or before a negative position */
+            for (int d = 0; d < D; ++d) out[r * D + d] = 0.0;
+            lse[r] = -INFINITY;
+        } else {
+            oracle_attend(qd, Kd, Vd, L, D, pos, 1, window, softcap, scale, out + r * D, lse + r);
+        }
+        free(qd); free(Kd); free(Vd);
+    }
+    return 0;
+}
+
 /* Number of threads OpenMP would use (for reporting the CPU baseline). */
 int oracle_max_threads(void)
 {

@@ -37,6 +37,8 @@ __all__ = [
     "make_decode_case",
     "make_prefill_case",
     "paged_from_contiguous",
+    "ChunkCase",
+    "make_chunked_case",
     "WORKLOADS",
 ]
 
@@ -159,6 +161,47 @@ class PrefillCase:
         return PrefillCase(**kw)
 
 
+@dataclass
+class ChunkCase:
+    """Inputs of one chunked-prefill / multi-token decode call over a paged cache.
+
+    Layouts (row-major):
+      q            f16 [total_q, Hq, D]: sequence b's new tokens are rows
+                   q_start[b] .. q_start[b+1]-1
+      k, v         f16 pool [n_pages, P, Hkv, D]; the new tokens' K/V are already
+                   the last q_len[b] of sequence b's kv_len[b] cache tokens
+      q_start      int32 [B+1]; kv_len int32 [B]; page_table int32 [B, max_pages]
+    """
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    q_start: torch.Tensor
+    kv_len: torch.Tensor
+    page_table: torch.Tensor
+    batch: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    page_size: int
+    max_pages: int
+    max_q: int
+    window: int = 0
+    softcap: float = 0.0
+    scale: float = 0.0
+    q_lens: list = field(default_factory=list)
+    kv_lens: list = field(default_factory=list)
+
+    @property
+    def total_q(self) -> int:
+        return int(sum(self.q_lens))
+
+    def to(self, device: str) -> "ChunkCase":
+        kw = dict(self.__dict__)
+        for name in ("q", "k", "v", "q_start", "kv_len", "page_table"):
+            kw[name] = kw[name].to(device)
+        return ChunkCase(**kw)
+
+
 def _lengths(batch: int, lo: int, hi: int, seed: int) -> list:
     g = _gen(seed * 7919 + 17, "cpu")
     return torch.randint(lo, hi + 1, (batch,), generator=g).tolist()
@@ -262,6 +305,49 @@ def paged_from_contiguous(case: DecodeCase, page_size: int, seed: int,
     kw.update(k=kp, v=vp, k_scales=ksp, v_scales=vsp, page_table=pt.to(dev),
               page_size=P, max_pages=max_pages, cap=max_pages * P)
     return DecodeCase(**kw)
+
+
+def make_chunked_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int, q_lens, ctx_lens,
+                      seed: int, *, page_size: int, n_pages: Optional[int] = None, window: int = 0,
+                      softcap: float = 0.0, scale: Optional[float] = None,
+                      device: str = "cpu") -> ChunkCase:
+    """Build a chunked-prefill case: sequence b has ctx_lens[b] cached tokens
+    before a chunk of q_lens[b] new ones (kv_len = ctx + q_len).  Either list may
+    be a (lo, hi) tuple for seeded uniform lengths.  Pages as in make_decode_case.
+    """
+    if isinstance(q_lens, tuple):
+        q_lens = _lengths(batch, q_lens[0], q_lens[1], seed * 3 + 1)
+    if isinstance(ctx_lens, tuple):
+        ctx_lens = _lengths(batch, ctx_lens[0], ctx_lens[1], seed * 3 + 2)
+    q_lens = [int(x) for x in q_lens]
+    kv_lens = [int(c) + int(n) for c, n in zip(ctx_lens, q_lens)]
+    assert len(q_lens) == batch and len(kv_lens) == batch
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    total_q = sum(q_lens)
+    q = f16_normal((max(total_q, 1), n_heads, head_dim), seed * 1000 + 21, device)
+    q_start = torch.tensor([0] + list(torch.tensor(q_lens).cumsum(0).tolist()), dtype=torch.int32,
+                           device=device)
+    P = page_size
+    need = [(L + P - 1) // P for L in kv_lens]
+    max_pages = max(max(need), 1)
+    if n_pages is None:
+        n_pages = max(sum(need), 1)
+    assert sum(need) <= n_pages
+    perm = torch.randperm(n_pages, generator=_gen(seed * 1000 + 24, "cpu"))
+    pt = torch.full((batch, max_pages), -1, dtype=torch.int32)
+    pos = 0
+    for b in range(batch):
+        pt[b, :need[b]] = perm[pos:pos + need[b]].to(torch.int32)
+        pos += need[b]
+    k = f16_normal((n_pages, P, n_kv_heads, head_dim), seed * 1000 + 22, device)
+    v = f16_normal((n_pages, P, n_kv_heads, head_dim), seed * 1000 + 23, device)
+    return ChunkCase(q=q, k=k, v=v, q_start=q_start,
+                     kv_len=torch.tensor(kv_lens, dtype=torch.int32, device=device),
+                     page_table=pt.to(device), batch=batch, n_heads=n_heads, n_kv_heads=n_kv_heads,
+                     head_dim=head_dim, page_size=P, max_pages=max_pages, max_q=max(max(q_lens), 1),
+                     window=window, softcap=softcap, scale=float(scale), q_lens=q_lens,
+                     kv_lens=kv_lens)
 
 
 def make_prefill_case(seq_len: int, n_heads: int, n_kv_heads: int, head_dim: int, seed: int, *,

@@ -369,3 +369,103 @@ def test_int8_encoding_rule():
     assert torch.all(cf[5] == 0) and sf[5] == 0
     err = (xf - cf * sf[:, None]).abs().max(dim=1).values
     assert torch.all(err <= sf * 0.5 * (1 + 1e-3) + 1e-12)
+
+
+# ---- chunked prefill / multi-token decode over a paged cache -----------------
+
+def _chunk_from_prefill(pc, page_size, seed):
+    """A one-sequence chunk holding all of a prefill case's tokens (ctx 0), with
+    its K/V scattered into a paged pool by a seeded permutation."""
+    S, Hkv, D, P = pc.seq_len, pc.n_kv_heads, pc.head_dim, page_size
+    max_pages = (S + P - 1) // P
+    n_pages = max_pages + 2
+    perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(seed))
+    pt = perm[:max_pages].view(1, max_pages).to(torch.int32)
+    kp = torch.zeros((n_pages, P, Hkv, D), dtype=torch.float16)
+    vp = torch.zeros((n_pages, P, Hkv, D), dtype=torch.float16)
+    for i in range(max_pages):
+        t0, t1 = i * P, min((i + 1) * P, S)
+        kp[int(pt[0, i]), :t1 - t0] = pc.k[t0:t1]
+        vp[int(pt[0, i]), :t1 - t0] = pc.v[t0:t1]
+    return si.ChunkCase(q=pc.q, k=kp, v=vp, q_start=torch.tensor([0, S], dtype=torch.int32),
+                        kv_len=torch.tensor([S], dtype=torch.int32), page_table=pt, batch=1,
+                        n_heads=pc.n_heads, n_kv_heads=Hkv, head_dim=D, page_size=P,
+                        max_pages=max_pages, max_q=S, window=pc.window, softcap=pc.softcap,
+                        scale=pc.scale, q_lens=[S], kv_lens=[S])
+
+
+@pytest.mark.parametrize("page_size", [1, 8, 16])
+@pytest.mark.parametrize("window", [0, 9])
+def test_whole_sequence_chunk_equals_causal_prefill(page_size, window):
+    # a chunk with no prior context is causal prefill of the same tokens: the
+    # page gather and the query positions must reproduce the contiguous path
+    pc = si.make_prefill_case(37, 4, 2, 32, seed=5, causal=True, window=window, softcap=3.0, scale=0.3)
+    cc = _chunk_from_prefill(pc, page_size, seed=7)
+    a, la = oracle.prefill(pc)
+    b, lb = oracle.prefill_paged(cc)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+def test_one_token_chunks_equal_decode():
+    # decode is the one-new-token case: the query sits at kv_len - 1
+    cc = si.make_chunked_case(3, 4, 2, 32, [1, 1, 1], [40, 0, 17], seed=11, page_size=8, window=10)
+    dc = si.DecodeCase(q=cc.q, k=cc.k, v=cc.v, kv_len=cc.kv_len, batch=3, n_heads=4, n_kv_heads=2,
+                       head_dim=32, cap=cc.max_pages * cc.page_size, page_table=cc.page_table,
+                       page_size=cc.page_size, max_pages=cc.max_pages, window=10, scale=cc.scale)
+    a, la = oracle.prefill_paged(cc)
+    b, lb = oracle.decode(dc)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+@pytest.mark.parametrize("window,softcap", [(0, 0.0), (6, 0.0), (0, 2.5)])
+def test_chunked_matches_brute_force(window, softcap):
+    # scipy softmax over the full score matrix with an independently built mask
+    cc = si.make_chunked_case(3, 4, 2, 16, [5, 1, 9], [11, 0, 20], seed=13, page_size=4,
+                              window=window, softcap=softcap, scale=0.4)
+    got, lse = oracle.prefill_paged(cc)
+    q = cc.q.double().numpy()
+    k, v, pt = cc.k.double().numpy(), cc.v.double().numpy(), cc.page_table.numpy()
+    P, G = cc.page_size, cc.n_heads // cc.n_kv_heads
+    row = 0
+    for b in range(cc.batch):
+        L, n = cc.kv_lens[b], cc.q_lens[b]
+        keys = np.stack([k[pt[b, t // P], t % P] for t in range(L)])     # [L, Hkv, D]
+        vals = np.stack([v[pt[b, t // P], t % P] for t in range(L)])
+        for i in range(n):
+            pos = L - n + i
+            for h in range(cc.n_heads):
+                s = cc.scale * keys[:, h // G, :] @ q[row + i, h]
+                if softcap > 0:
+                    s = softcap * np.tanh(s / softcap)
+                t = np.arange(L)
+                keep = t <= pos
+                if window > 0:
+                    keep &= (pos - t) < window
+                s = np.where(keep, s, -np.inf)
+                p = scipy.special.softmax(s)
+                r = (row + i) * cc.n_heads + h
+                np.testing.assert_allclose(got[r], p @ vals[:, h // G, :], rtol=0, atol=1e-12)
+                np.testing.assert_allclose(lse[r], scipy.special.logsumexp(s), rtol=0, atol=1e-12)
+        row += n
+
+
+def test_chunk_longer_than_its_cache_sees_nothing_before_position_zero():
+    # kv_len < q_len: the first q_len - kv_len queries sit at negative positions
+    cc = si.make_chunked_case(1, 2, 1, 16, [6], [0], seed=17, page_size=4)
+    cc.kv_len = torch.tensor([4], dtype=torch.int32)     # only 4 of the 6 tokens are cached
+    got, lse = oracle.prefill_paged(cc)
+    got, lse = got.reshape(6, 2, 16), lse.reshape(6, 2)
+    assert np.all(got[:2] == 0) and np.all(np.isneginf(lse[:2]))
+    # query 2 sits at position 0 and sees key 0 only: its value row
+    v0 = cc.v[int(cc.page_table[0, 0]), 0, 0].double().numpy()
+    np.testing.assert_allclose(got[2, 0], v0, rtol=0, atol=1e-12)
+
+
+def test_empty_chunks_are_skipped():
+    cc = si.make_chunked_case(3, 2, 2, 16, [0, 3, 0], [10, 5, 0], seed=19, page_size=4)
+    got, _ = oracle.prefill_paged(cc)
+    assert got.shape == (3 * 2, 16)
+    ref, _ = oracle.prefill_paged(si.make_chunked_case(3, 2, 2, 16, [0, 3, 0], [10, 5, 0], seed=19,
+                                                       page_size=4), rows=[(r, h) for r in range(3)
+                                                                          for h in range(2)])
+    assert np.array_equal(got, ref)
