@@ -19,8 +19,8 @@ __all__ = [
     "ATTN_KV_F16", "ATTN_KV_INT8", "AttnError", "AttnLibraryMissing",
     "lib_path", "load", "build", "exported_symbols",
     "attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-    "attn_decode_noalloc", "attn_prefill", "attn_decode_validate", "attn_device_status",
-    "decode", "prefill",
+    "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate", "attn_device_status",
+    "decode", "prefill", "prefill_paged",
 ]
 
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_EBOUNDS, ATTN_ETIMEOUT = range(6)
@@ -34,7 +34,8 @@ _lib = None
 
 # every entry point include/attn.h declares
 exported_symbols = ("attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-                    "attn_decode_noalloc", "attn_prefill", "attn_decode_validate", "attn_device_status")
+                    "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate",
+                    "attn_device_status")
 
 
 class AttnLibraryMissing(RuntimeError):
@@ -75,6 +76,8 @@ def load():
     lib.attn_decode_noalloc.restype = I
     lib.attn_prefill.argtypes = [P, P, P, I, I, I, I, I, I, F, F, P, P, P]
     lib.attn_prefill.restype = I
+    lib.attn_prefill_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, F, P, P, P]
+    lib.attn_prefill_paged.restype = I
     lib.attn_decode_validate.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(ctypes.c_int), P]
     lib.attn_decode_validate.restype = I
     lib.attn_device_status.argtypes = [P]
@@ -196,4 +199,25 @@ def prefill(case, out=None, lse_out=None, stream=None):
         out = torch.empty_like(case.q)
     attn_prefill(case.q, case.k, case.v, case.seq_len, case.n_heads, case.n_kv_heads, case.head_dim,
                  case.causal, case.window, case.softcap, case.scale, out, lse_out, stream)
+    return out
+
+
+def attn_prefill_paged(q, k_cache, v_cache, q_start, kv_len, page_table, page_size, max_pages, n_pages, batch,
+                       total_q, max_q, n_heads, n_kv_heads, head_dim, window, softcap, scale, out, lse_out,
+                       stream=None) -> None:
+    _check(load().attn_prefill_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(q_start), _ptr(kv_len),
+                                     _ptr(page_table), int(page_size), int(max_pages), int(n_pages), int(batch),
+                                     int(total_q), int(max_q), int(n_heads), int(n_kv_heads), int(head_dim),
+                                     int(window), float(softcap), float(scale), _ptr(out), _ptr(lse_out),
+                                     _stream(stream)))
+
+
+def prefill_paged(case, out=None, lse_out=None, stream=None):
+    """attn_prefill_paged on a ChunkCase-like object (tensors already on the GPU)."""
+    import torch
+    if out is None:
+        out = torch.empty_like(case.q)
+    attn_prefill_paged(case.q, case.k, case.v, case.q_start, case.kv_len, case.page_table, case.page_size,
+                       case.max_pages, int(case.k.shape[0]), case.batch, case.total_q, case.max_q, case.n_heads,
+                       case.n_kv_heads, case.head_dim, case.window, case.softcap, case.scale, out, lse_out, stream)
     return out

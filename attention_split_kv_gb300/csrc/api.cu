@@ -296,6 +296,68 @@ attn_status attn_prefill(const void* q, const void* k, const void* v, int seq_le
     return launch_prefill(L);
 }
 
+attn_status attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* q_start,
+                               const int32_t* kv_len, const int32_t* page_table, int page_size,
+                               int max_pages_per_seq, int n_pages, int batch, int total_q, int max_q, int n_heads,
+                               int n_kv_heads, int head_dim, int window, float softcap, float scale, void* out,
+                               float* lse_out, void* stream) {
+    if (!q || !k_cache || !v_cache || !q_start || !kv_len || !page_table || !out)
+        return set_error(ATTN_EINVAL, "attn_prefill_paged: q, caches, q_start, kv_len, page_table and out must be "
+                                      "non-null");
+    if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0 || total_q < 0 || max_q < 0)
+        return set_error(ATTN_EINVAL, "attn_prefill_paged: positive batch and head counts, total_q/max_q >= 0 "
+                                      "required");
+    if (n_heads % n_kv_heads != 0)
+        return set_error(ATTN_EINVAL, "attn_prefill_paged: n_heads (%d) must be a multiple of n_kv_heads (%d)",
+                         n_heads, n_kv_heads);
+    if (n_heads > 65535 || batch > 65535)
+        return set_error(ATTN_EUNSUPPORTED, "attn_prefill_paged: n_heads and batch must be at most 65535");
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return set_error(ATTN_EUNSUPPORTED, "attn_prefill_paged: head_dim %d not supported (64, 128, 256)",
+                         head_dim);
+    if (page_size < 8 || (page_size & (page_size - 1)) != 0)
+        return set_error(ATTN_EUNSUPPORTED, "attn_prefill_paged: page_size %d must be a power of two >= 8",
+                         page_size);
+    if (max_pages_per_seq <= 0 || n_pages <= 0)
+        return set_error(ATTN_EINVAL, "attn_prefill_paged: max_pages_per_seq and n_pages must be positive");
+    if (window < 0) return set_error(ATTN_EINVAL, "attn_prefill_paged: window must be >= 0 (0 = off)");
+    if (!(softcap >= 0.f) || !std::isfinite(softcap))
+        return set_error(ATTN_EINVAL, "attn_prefill_paged: softcap must be finite and >= 0 (0 = off)");
+    if (!std::isfinite(scale)) return set_error(ATTN_EINVAL, "attn_prefill_paged: scale must be finite");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return set_error(ATTN_EINVAL, "attn_prefill_paged: q, caches and out must be 16-byte aligned");
+    if (total_q == 0 || max_q == 0) return ATTN_OK;
+    int* err = device_error_word();
+    if (!err) return set_error(ATTN_ECUDA, "attn_prefill_paged: no CUDA device / error word");
+    PrefillLaunch L;
+    L.q = q;
+    L.k = k_cache;
+    L.v = v_cache;
+    L.out = out;
+    L.lse = lse_out;
+    L.S = 0;
+    L.Hq = n_heads;
+    L.Hkv = n_kv_heads;
+    L.D = head_dim;
+    L.causal = 1;
+    L.window = window;
+    L.softcap = softcap;
+    L.scale = scale;
+    L.err_word = err;
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.paged = 1;
+    L.q_start = q_start;
+    L.kv_len = kv_len;
+    L.page_table = page_table;
+    L.page_size = page_size;
+    L.max_pages = max_pages_per_seq;
+    L.n_pages = n_pages;
+    L.B = batch;
+    L.total_q = total_q;
+    L.max_q = max_q;
+    return launch_prefill(L);
+}
+
 attn_status attn_decode_validate(const int32_t* kv_len, const int32_t* page_table, int batch, int page_size,
                                  int max_pages_per_seq, int n_pages, int max_kv, int* bad_seq, void* stream) {
     if (!kv_len || batch <= 0 || max_kv <= 0)

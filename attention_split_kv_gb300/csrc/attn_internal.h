@@ -55,6 +55,12 @@ struct PrefillLaunch {
     float softcap, scale;
     int* err_word;
     cudaStream_t stream;
+    // chunks over a paged cache (paged != 0): k/v are the page pool
+    int paged = 0;
+    const int32_t* q_start = nullptr;
+    const int32_t* kv_len = nullptr;
+    const int32_t* page_table = nullptr;
+    int page_size = 0, max_pages = 0, n_pages = 0, B = 0, total_q = 0, max_q = 0;
 };
 attn_status launch_prefill(const PrefillLaunch& L);
 

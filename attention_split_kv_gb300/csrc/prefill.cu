@@ -162,9 +162,17 @@ struct PrefillArgs {
     int S, Hq, Hkv, causal, window;
     float softcap, scale;
     int* err;
+    // paged chunks only: sequence b's queries are packed rows q_start[b] ..
+    // q_start[b+1]-1 at positions kv_len[b] - q_len + i over its kv_len[b] cached
+    // keys, read through the page table in boxes of box_rows rows
+    const int32_t* q_start;
+    const int32_t* kv_len;
+    const int32_t* page_table;
+    int P, log2P, max_pages, n_pages, box_rows;
+    int total_q;       // rows of q/out (S for contiguous prefill)
 };
 
-template <int D, int MODE>
+template <int D, int MODE, bool PAGED>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, PrefillCfg<D>::CTAS_PER_SM)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
@@ -186,20 +194,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     constexpr int NBUF = C::NBUF;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = args.S;
-    const int n_qt = (S + BM - 1) / BM;
+    // Geometry.  Queries i in [0, n_q) of one sequence sit at positions pos0 + i
+    // over keys [0, L); contiguous prefill has one sequence of S tokens with
+    // positions 0 .. S-1, a paged chunk the last n_q of its sequence's tokens.
+    int n_q = args.S, L = args.S, pos0 = 0, q_base = 0, b = 0;
+    if constexpr (PAGED) {
+        b = blockIdx.z;
+        q_base = args.q_start[b];
+        n_q = args.q_start[b + 1] - q_base;
+        const int kvl = args.kv_len[b];
+        L = min(max(kvl, 0), args.max_pages * args.P);
+        pos0 = kvl - n_q;
+    }
+    const int n_qt = (n_q + BM - 1) / BM;
     // causal tiles late in the sequence carry the most keys: launch them first
-    const int qt = args.causal ? (n_qt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    const int qt = PAGED ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                         : (args.causal ? (n_qt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
+    if (PAGED && qt >= n_qt) return;   // a shorter chunk: no queries for this CTA
     const int h = blockIdx.y;
     const int g = h / (args.Hq / args.Hkv);
     const int q0 = qt * BM;
-    const int q_last = min(q0 + BM - 1, S - 1);
+    const int q_last = min(q0 + BM - 1, n_q - 1);
     const int W = args.window;
-    int hi = args.causal ? q_last + 1 : S;
-    if (!args.causal && W > 0) hi = min(S, q_last + W);
-    const int lo = W > 0 ? max(0, q0 - W + 1) : 0;
+    int hi = args.causal ? min(L, pos0 + q_last + 1) : L;
+    if (!args.causal && W > 0) hi = min(L, q_last + W);
+    const int lo = W > 0 ? max(0, pos0 + q0 - W + 1) : 0;
     const int jt0 = lo / BN;
-    const int n_tiles = (hi + BN - 1) / BN - jt0;
+    const int n_tiles = hi > lo ? (hi + BN - 1) / BN - jt0 : 0;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_QFULL), 1);
@@ -246,7 +267,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tma_prefetch_desc(&tm_q);
                     mbar_arrive_expect_tx(bar(B_QFULL), C::Q_BYTES);
                     for (int c = 0; c < NCH; ++c)
-                        tma_load_3d(sbase + C::OFF_Q + c * (BM * 128), &tm_q, bar(B_QFULL), c * 64, h, q0);
+                        tma_load_3d(sbase + C::OFF_Q + c * (BM * 128), &tm_q, bar(B_QFULL), c * 64, h, q_base + q0);
                 }
                 int issued = 0;
                 for (int j = 0; j < n_tiles; ++j) {
@@ -256,8 +277,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         break;
                     const int key0 = (jt0 + j) * BN;
                     mbar_arrive_expect_tx(bar(b_full + st), C::KV_BYTES);
-                    for (int c = 0; c < NCH; ++c)
-                        tma_load_3d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK, tm, bar(b_full + st), c * 64, g, key0);
+                    if constexpr (PAGED) {
+                        // one box of box_rows rows per page (or one box inside a page);
+                        // boxes past the cached keys get the page coordinate n_pages, past
+                        // the pool, so the copy fills zeros instead of reading anything
+                        const int R = args.box_rows;
+                        for (int i = 0; i * R < BN; ++i) {
+                            const int kk = key0 + i * R;
+                            int page = args.n_pages, row = 0;
+                            if (kk < L) {
+                                const int pid = __ldg(&args.page_table[(size_t)b * args.max_pages + (kk >> args.log2P)]);
+                                if (pid >= 0 && pid < args.n_pages) page = pid;
+                                else atomicExch(args.err, kErrBadPage);   // never read: reported
+                                row = kk & (args.P - 1);
+                            }
+                            for (int c = 0; c < NCH; ++c)
+                                tma_load_4d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK + i * R * 128, tm,
+                                            bar(b_full + st), c * 64, g, row, page);
+                        }
+                    } else {
+                        for (int c = 0; c < NCH; ++c)
+                            tma_load_3d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK, tm, bar(b_full + st), c * 64,
+                                        g, key0);
+                    }
                     issued = j + 1;
                 }
                 if (*abort_flag) {
@@ -332,7 +374,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ------------------------------------------------------------ softmax warps
         if constexpr (C::THREADS == 256) setmaxnreg_inc<C::REG_SOFTMAX>();
         const int row = threadIdx.x;           // 0..127 == TMEM lane
-        const int qi = q0 + row;
+        const int qi = q0 + row;             // query index within the sequence
+        const int pos = pos0 + qi;           // its position among the keys
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         const float scale_log2 = args.scale * kLog2e;
         const float cap_log2 = args.softcap * kLog2e;
@@ -355,9 +398,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             const int key0 = (jt0 + j) * BN;
             const int key_last = key0 + BN - 1;
-            bool full = key_last < S;
-            if (args.causal) full = full && key_last <= qi;
-            if (W > 0) full = full && (qi - key0 < W) && (args.causal || key_last - qi < W);
+            bool full = key_last < L;
+            if (args.causal) full = full && key_last <= pos;
+            if (W > 0) full = full && (pos - key0 < W) && (args.causal || key_last - pos < W);
             // logits in log2 units (the raw mode keeps accumulators and scales in the exponent)
             if constexpr (MODE == kModeCapped) {
                 // c*tanh(s/c): the odd Taylor polynomial through x^9 on the FMA pipe
@@ -403,10 +446,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                 for (int i = 0; i < BN; ++i) {
                     const int kj = key0 + i;
-                    bool keep = kj < S;
-                    if (args.causal) keep = keep && kj <= qi;
+                    bool keep = kj < L;
+                    if (args.causal) keep = keep && kj <= pos;
                     if (W > 0) {
-                        int dist = qi - kj;
+                        int dist = pos - kj;
                         if (!args.causal && dist < 0) dist = -dist;
                         keep = keep && dist < W;
                     }
@@ -468,6 +511,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tc_st_32x32b_x32(lane_base + C::COL_O + c * 32, r);
                 }
             }
+            if constexpr (PAGED) {
+                if (key0 + BN > L) {
+                    // keys past the cache: zero their V rows, since the cache may hold
+                    // anything there and P = 0 must not meet a NaN
+                    const int stv = j % C::VST;
+                    if (!mbar_wait(bar(B_VFULL + stv), (j / C::VST) & 1, abort_flag, args.err, kErrTimeoutLoad)) {
+                        ok = false;
+                        break;
+                    }
+                    const int r0 = max(L - key0, 0);
+                    const int per_chunk = (BN - r0) * 8;          // 16-byte units per chunk
+                    uint8_t* vt = smem + C::OFF_V + stv * C::KV_BYTES;
+                    for (int u = row; u < NCH * per_chunk; u += BM) {
+                        const int c = u / per_chunk, rem = u - c * per_chunk;
+                        *reinterpret_cast<uint4*>(vt + c * C::KV_CHUNK + (r0 + rem / 8) * 128 + (rem % 8) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
             tc_wait_st();
             tc_fence_before();
             mbar_arrive(bar(B_PFULL + (j % NBUF)));
@@ -480,13 +543,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (ok) {
             tc_fence_after();
             const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-            __half* orow = args.out + (static_cast<size_t>(qi) * args.Hq + h) * D;
+            // a row of this chunk, inside q/out even if q_start disagrees with total_q
+            const bool row_ok = qi < n_q && q_base + qi >= 0 && q_base + qi < args.total_q;
+            __half* orow = args.out + (static_cast<size_t>(q_base + qi) * args.Hq + h) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
-                tc_ld_32x32b_x32(lane_base + C::COL_O + c * 32, r);
-                tc_wait_ld();
-                if (qi < S) {
+                if (n_tiles > 0) {
+                    tc_ld_32x32b_x32(lane_base + C::COL_O + c * 32, r);
+                    tc_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = 0u;   // no key at all: O was never written
+                }
+                if (row_ok) {
                     uint32_t hv[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -499,8 +569,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
                 }
             }
-            if (args.lse && qi < S) {
-                args.lse[static_cast<size_t>(qi) * args.Hq + h] =
+            if (args.lse && row_ok) {
+                args.lse[static_cast<size_t>(q_base + qi) * args.Hq + h] =
                     l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
             }
         }
@@ -513,20 +583,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool PAGED>
 attn_status launch_prefill_dm(const PrefillLaunch& L) {
     using C = PrefillCfg<D>;
     CUtensorMap tq, tk, tv;
     attn_status st;
-    // 3-D maps over [S, H, D] f16: dims (D, H, S), 64-element x rows boxes, 128-byte swizzle
-    if ((st = encode_tmap_3d_f16_sw128(&tq, L.q, D, L.Hq, L.S, BM)) != ATTN_OK) return st;
-    if ((st = encode_tmap_3d_f16_sw128(&tk, L.k, D, L.Hkv, L.S, C::BN)) != ATTN_OK) return st;
-    if ((st = encode_tmap_3d_f16_sw128(&tv, L.v, D, L.Hkv, L.S, C::BN)) != ATTN_OK) return st;
+    int box_rows = C::BN;
+    if (!PAGED) {
+        // 3-D maps over [S, H, D] f16: dims (D, H, S), 64-element x rows boxes, 128-byte swizzle
+        if ((st = encode_tmap_3d_f16_sw128(&tq, L.q, D, L.Hq, L.S, BM)) != ATTN_OK) return st;
+        if ((st = encode_tmap_3d_f16_sw128(&tk, L.k, D, L.Hkv, L.S, C::BN)) != ATTN_OK) return st;
+        if ((st = encode_tmap_3d_f16_sw128(&tv, L.v, D, L.Hkv, L.S, C::BN)) != ATTN_OK) return st;
+    } else {
+        // q [total_q, Hq, D] as above; the pool [n_pages, P, Hkv, D] as (D, Hkv, P, n_pages)
+        // with boxes of (64, 1 head, min(P, tile keys) rows, 1 page)
+        if ((st = encode_tmap_3d_f16_sw128(&tq, L.q, D, L.Hq, L.total_q, BM)) != ATTN_OK) return st;
+        box_rows = L.page_size < C::BN ? L.page_size : C::BN;
+        const uint64_t dims[4] = {(uint64_t)D, (uint64_t)L.Hkv, (uint64_t)L.page_size, (uint64_t)L.n_pages};
+        const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)D * 2 * L.Hkv,
+                                     (uint64_t)D * 2 * L.Hkv * L.page_size};
+        const uint32_t box[4] = {64u, 1u, (uint32_t)box_rows, 1u};
+        if ((st = encode_tmap_sw128(&tk, L.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, dims, strides, box)) != ATTN_OK)
+            return st;
+        if ((st = encode_tmap_sw128(&tv, L.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, dims, strides, box)) != ATTN_OK)
+            return st;
+    }
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(prefill_tc_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_tc_kernel<D, MODE, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_ALLOC) != cudaSuccess)
             return set_error(ATTN_ECUDA, "cudaFuncSetAttribute(prefill smem) failed");
         attr_set[dev] = true;
@@ -542,29 +628,44 @@ attn_status launch_prefill_dm(const PrefillLaunch& L) {
     a.softcap = L.softcap;
     a.scale = L.scale;
     a.err = L.err_word;
-    dim3 grid((L.S + BM - 1) / BM, L.Hq);
-    prefill_tc_kernel<D, MODE><<<grid, C::THREADS, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
+    a.q_start = L.q_start;
+    a.kv_len = L.kv_len;
+    a.page_table = L.page_table;
+    a.P = L.page_size;
+    a.log2P = 0;
+    while ((1 << a.log2P) < L.page_size) ++a.log2P;
+    a.max_pages = L.max_pages;
+    a.n_pages = L.n_pages;
+    a.box_rows = box_rows;
+    a.total_q = PAGED ? L.total_q : L.S;
+    const dim3 grid = PAGED ? dim3((L.max_q + BM - 1) / BM, L.Hq, L.B) : dim3((L.S + BM - 1) / BM, L.Hq);
+    prefill_tc_kernel<D, MODE, PAGED><<<grid, C::THREADS, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }
 
-template <int D>
+template <int D, bool PAGED>
 attn_status launch_prefill_d(const PrefillLaunch& L) {
-    if (L.softcap > 0.f) return launch_prefill_dm<D, kModeCapped>(L);
-    if (L.scale > 0.f) return launch_prefill_dm<D, kModeRaw>(L);
-    return launch_prefill_dm<D, kModeScaled>(L);
+    if (L.softcap > 0.f) return launch_prefill_dm<D, kModeCapped, PAGED>(L);
+    if (L.scale > 0.f) return launch_prefill_dm<D, kModeRaw, PAGED>(L);
+    return launch_prefill_dm<D, kModeScaled, PAGED>(L);
+}
+
+template <bool PAGED>
+attn_status launch_prefill_p(const PrefillLaunch& L) {
+    switch (L.D) {
+        case 64: return launch_prefill_d<64, PAGED>(L);
+        case 128: return launch_prefill_d<128, PAGED>(L);
+        case 256: return launch_prefill_d<256, PAGED>(L);
+        default: return set_error(ATTN_EUNSUPPORTED, "head_dim %d not supported (64, 128, 256)", L.D);
+    }
 }
 
 }  // namespace
 
 attn_status launch_prefill(const PrefillLaunch& L) {
-    switch (L.D) {
-        case 64: return launch_prefill_d<64>(L);
-        case 128: return launch_prefill_d<128>(L);
-        case 256: return launch_prefill_d<256>(L);
-        default: return set_error(ATTN_EUNSUPPORTED, "head_dim %d not supported (64, 128, 256)", L.D);
-    }
+    return L.paged ? launch_prefill_p<true>(L) : launch_prefill_p<false>(L);
 }
 
 }  // namespace attn

@@ -165,6 +165,47 @@ attn_status attn_prefill(const void* q, const void* k, const void* v,
                          void* out, float* lse_out, void* stream);
 
 /*
+ * attn_prefill_paged -- chunked prefill / multi-token decode: each sequence
+ * appends a chunk of new tokens to its paged KV cache and the chunk's queries
+ * attend causally to every cached token up to their own position
+ * (doppler attention.js, createAttentionUniformBuffer: seqLen new tokens at
+ * startPos over kvLen keys with the paged layout's page table and pageSize;
+ * attn_decode is the one-token case).  Same tensor-core kernel as
+ * attn_prefill, with K/V read through the page table.
+ *
+ *  q         device f16 [total_q, Hq, D]: sequence b's new tokens are the rows
+ *            q_start[b] .. q_start[b+1]-1 (packed, sequences in order).
+ *  k_cache, v_cache  device f16 page pool [n_pages, P, Hkv, D].  The chunk's
+ *            own K/V must already be written: they are the last q_len of the
+ *            sequence's kv_len tokens.
+ *  q_start   device i32 [B+1], non-decreasing, q_start[0] = 0, q_start[B] = total_q.
+ *  kv_len    device i32 [B]: cached tokens of each sequence, chunk included.
+ *            Query i of sequence b (q_len = q_start[b+1] - q_start[b]) sits at
+ *            position kv_len[b] - q_len + i and keeps keys j <= position
+ *            (and position - j < window when window > 0).  Keys at or above
+ *            max_pages_per_seq * P are clamped away (as in attn_decode); a
+ *            query at a negative position keeps no key: out = 0, lse = -inf.
+ *  page_table  device i32 [B, max_pages_per_seq]: logical token t of sequence b
+ *            is row t % P of page page_table[b][t / P].  A page id in use that
+ *            lies outside [0, n_pages) is never read (its keys read as zeros)
+ *            and is reported through attn_device_status (ATTN_EBOUNDS).
+ *  page_size P: a power of two >= 8.
+ *  total_q   rows of q; max_q: an upper bound of q_len over the sequences
+ *            (sizes the launch; a chunk longer than max_q is cut at max_q rows).
+ *  softcap, scale  as in attn_decode.
+ *  out       device f16 [total_q, Hq, D]; lse_out device f32 [total_q, Hq] or NULL.
+ *  D must be 64, 128 or 256; base addresses 16-byte aligned.  Asynchronous on
+ *  `stream`; the host reads none of the device arrays.
+ */
+attn_status attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* q_start, const int32_t* kv_len, const int32_t* page_table,
+                               int page_size, int max_pages_per_seq, int n_pages,
+                               int batch, int total_q, int max_q,
+                               int n_heads, int n_kv_heads, int head_dim,
+                               int window, float softcap, float scale,
+                               void* out, float* lse_out, void* stream);
+
+/*
  * attn_decode_validate -- synchronous check of the device-side decode inputs:
  * every kv_len[b] in [1, capacity] and every page id a sequence uses in
  * [0, n_pages).  Launches one small kernel on stream and waits for it.

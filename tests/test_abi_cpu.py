@@ -127,3 +127,39 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(attn, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(attn.AttnLibraryMissing):
         attn.attn_version()
+
+
+def _prefill_paged(**kw):
+    args = dict(q=FAKE, k_cache=FAKE, v_cache=FAKE, q_start=FAKE, kv_len=FAKE, page_table=FAKE, page_size=16,
+                max_pages=4, n_pages=8, batch=2, total_q=10, max_q=8, n_heads=4, n_kv_heads=2, head_dim=64,
+                window=0, softcap=0.0, scale=0.125, out=FAKE, lse_out=None, stream=0)
+    args.update(kw)
+    return attn.load().attn_prefill_paged(*[args[k] for k in (
+        "q", "k_cache", "v_cache", "q_start", "kv_len", "page_table", "page_size", "max_pages", "n_pages",
+        "batch", "total_q", "max_q", "n_heads", "n_kv_heads", "head_dim", "window", "softcap", "scale", "out",
+        "lse_out", "stream")])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q_start=None), attn.ATTN_EINVAL),
+    (dict(page_table=None), attn.ATTN_EINVAL),
+    (dict(batch=0), attn.ATTN_EINVAL),
+    (dict(total_q=-1), attn.ATTN_EINVAL),
+    (dict(n_heads=5), attn.ATTN_EINVAL),
+    (dict(head_dim=80), attn.ATTN_EUNSUPPORTED),
+    (dict(page_size=12), attn.ATTN_EUNSUPPORTED),
+    (dict(page_size=4), attn.ATTN_EUNSUPPORTED),
+    (dict(n_pages=0), attn.ATTN_EINVAL),
+    (dict(window=-2), attn.ATTN_EINVAL),
+    (dict(softcap=float("nan")), attn.ATTN_EINVAL),
+    (dict(scale=float("inf")), attn.ATTN_EINVAL),
+    (dict(out=FAKE + 2), attn.ATTN_EINVAL),
+])
+def test_prefill_paged_rejects_bad_arguments_on_the_host(lib, kw, status):
+    assert _prefill_paged(**kw) == status
+    assert "attn_prefill_paged" in attn.attn_last_error()
+
+
+def test_prefill_paged_with_no_queries_is_a_no_op(lib):
+    assert _prefill_paged(total_q=0) == attn.ATTN_OK
+    assert _prefill_paged(max_q=0) == attn.ATTN_OK
