@@ -52,7 +52,8 @@ NCU_TRAFFIC = {
     "int8_long_decode": (136.53e6 + 8.45e6) * 8,
 }
 METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
-WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode"]
+WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode",
+                  "chunked_prefill_paged"]
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -87,6 +88,20 @@ def prefill_flops(case):
     return 4.0 * case.head_dim * live_pairs(case.seq_len, case.causal, case.window) * case.n_heads
 
 
+def chunk_flops(case):
+    """Chunked prefill: 4*D flops per kept (query, key) pair and query head; query i of
+    a chunk of n at the end of L cached keys sits at L - n + i and keeps the keys up to it."""
+    pairs = 0
+    for n, L in zip(case.q_lens, case.kv_lens):
+        for i in range(n):
+            pos = L - n + i
+            if pos < 0:
+                continue
+            lo = 0 if case.window <= 0 else max(0, pos - case.window + 1)
+            pairs += min(pos, L - 1) - lo + 1
+    return 4.0 * case.head_dim * pairs * case.n_heads
+
+
 def decode_bytes(case):
     """KV bytes a decode call must read once, plus q, out, kv_len and page table."""
     esz = 1 if case.int8 else 2
@@ -103,6 +118,11 @@ def decode_bytes(case):
 
 
 def workload_config(case):
+    if hasattr(case, "q_lens"):
+        return {"global_batch": case.batch, "chunk_tokens": case.total_q, "n_heads": case.n_heads,
+                "n_kv_heads": case.n_kv_heads, "head_dim": case.head_dim, "kv_len_min": min(case.kv_lens),
+                "kv_len_max": max(case.kv_lens), "page_size": case.page_size, "causal": True,
+                "window": case.window, "softcap": case.softcap}
     if hasattr(case, "seq_len"):
         return {"seq_len": case.seq_len, "n_heads": case.n_heads, "n_kv_heads": case.n_kv_heads,
                 "head_dim": case.head_dim, "causal": bool(case.causal), "window": case.window,
@@ -314,6 +334,10 @@ def main(argv=None):
             out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float16, device=dev)
             runs[n] = (lambda c=c, ws=ws, out=out: attn.decode(c, out=out, workspace=ws))
             work[n] = ("GB/s", decode_bytes(c), "hbm", 2)
+        elif si.WORKLOADS[n]["kind"] == "chunked":
+            out = torch.empty_like(c.q)
+            runs[n] = (lambda c=c, out=out: attn.prefill_paged(c, out=out))
+            work[n] = ("TFLOP/s", chunk_flops(c), "tensor", 1)
         else:
             out = torch.empty_like(c.q)
             runs[n] = (lambda c=c, out=out: attn.prefill(c, out=out))

@@ -381,6 +381,11 @@ WORKLOADS = {
     "int8_long_decode": dict(kind="decode", seed=5, batch=16, n_heads=32, n_kv_heads=8,
                              head_dim=128, lens=[32768] * 16, int8=True, page_size=0,
                              window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
+    # chunked prefill over a paged cache: 8 sequences append 512-token chunks to
+    # 512..7680 cached tokens (16-token pages), the GQA shape of the paged decode
+    "chunked_prefill_paged": dict(kind="chunked", seed=6, batch=8, n_heads=32, n_kv_heads=8,
+                                  head_dim=128, q_lens=[512] * 8, ctx_lens=(512, 7680), page_size=16,
+                                  window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
 }
 
 # Reduced cases of the same kernels for ncu captures (inputs still larger than
@@ -404,5 +409,8 @@ def make_workload(name: str, device: str = "cpu"):
         b, hq, hkv, d, lens = (w.pop("batch"), w.pop("n_heads"), w.pop("n_kv_heads"),
                                w.pop("head_dim"), w.pop("lens"))
         return make_decode_case(b, hq, hkv, d, lens, seed, device=device, **w)
+    if kind == "chunked":
+        b, hq, hkv, d = w.pop("batch"), w.pop("n_heads"), w.pop("n_kv_heads"), w.pop("head_dim")
+        return make_chunked_case(b, hq, hkv, d, w.pop("q_lens"), w.pop("ctx_lens"), seed, device=device, **w)
     s, hq, hkv, d = w.pop("seq_len"), w.pop("n_heads"), w.pop("n_kv_heads"), w.pop("head_dim")
     return make_prefill_case(s, hq, hkv, d, seed, device=device, **w)

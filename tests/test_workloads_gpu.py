@@ -1,4 +1,4 @@
-"""The five seeded workloads at full size, in the launch configuration the
+"""The seeded workloads at full size, in the launch configuration the
 benchmark times, checked against the oracle on sampled output rows (the
 oracle computes each sampled (query, head) row exactly, one by one)."""
 import numpy as np
@@ -66,3 +66,18 @@ def test_prefill_workload(name):
     got_lse = np.array([l[i, h] for i, h in rows])
     assert_close(got, ref, what=name)
     assert_lse_close(got_lse, ref_lse, what=name)
+
+
+def test_chunked_prefill_workload():
+    g = si.make_workload("chunked_prefill_paged", device="cuda")
+    lse = torch.empty((g.total_q, g.n_heads), dtype=torch.float32, device="cuda")
+    out = attn.prefill_paged(g, lse_out=lse)
+    torch.cuda.synchronize()
+    rows = _sample_rows(g.total_q, g.n_heads, 48, seed=6)
+    ref, ref_lse = oracle.prefill_paged(g.to("cpu"), rows=rows)
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    got = np.stack([o[i, h] for i, h in rows])
+    got_lse = np.array([l[i, h] for i, h in rows])
+    assert_close(got, ref, what="chunked_prefill_paged")
+    assert_lse_close(got_lse, ref_lse, what="chunked_prefill_paged")
