@@ -17,7 +17,7 @@
 //                                               V in smem as the MN-major operand)
 //
 // Roles: warps 0-3 softmax + epilogue (thread t owns query row t = TMEM lane
-// t), warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer (D=64 adds two
+// t), warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer (D=64/128 add two
 // idle warps 6-7 to complete the second warpgroup for setmaxnreg).
 // The MMA warp issues S_{j+1} before waiting for P_j, so QK^T of the next tile
 // overlaps the softmax of the current one.  O is rescaled lazily: only when a
@@ -44,24 +44,27 @@ enum : int { kModeRaw = 0, kModeScaled = 1, kModeCapped = 2 };
 template <int D>
 struct PrefillCfg {
     static constexpr int NCH = D / 64;                   // 64-element (128-byte) chunks of D
-    // D=64 runs two CTAs per SM (256 TMEM columns each) so that two softmax
-    // warpgroups share every SM; D=128/256 run one CTA per SM.
-    static constexpr int CTAS_PER_SM = (D == 64) ? 2 : 1;
-    // D=64: two full warpgroups, so that setmaxnreg can move registers from
-    // the producer/MMA warpgroup (warps 4-7, two of them idle) to the softmax
-    // warpgroup: 2 CTAs x 256 threads x 128 registers at launch, then
-    // 128 x 200 + 128 x 56 per CTA.  D=128/256 (one CTA per SM) run 6 warps.
-    static constexpr int THREADS = (D == 64) ? 256 : 192;
+    // D=64/128 run two CTAs per SM (256 TMEM columns each) so that two softmax
+    // warpgroups share every SM; D=256 runs one CTA per SM.
+    static constexpr int CTAS_PER_SM = (D <= 128) ? 2 : 1;
+    // D=64/128: two full warpgroups, so that setmaxnreg can move registers
+    // from the producer/MMA warpgroup (warps 4-7, two of them idle) to the
+    // softmax warpgroup: 2 CTAs x 256 threads x 128 registers at launch, then
+    // 128 x 200 + 128 x 56 per CTA.  D=256 (one CTA per SM) runs 6 warps.
+    static constexpr int THREADS = (D <= 128) ? 256 : 192;
     static constexpr int REG_SOFTMAX = 200, REG_OTHER = 56;
-    static_assert(D != 64 || (REG_SOFTMAX + REG_OTHER) * 128 * CTAS_PER_SM == 65536, "register split");
-    static constexpr int BN = (D == 256) ? 64 : 128;     // keys per tile
-    // S and P buffers in TMEM.  D=64 (two CTAs per SM, 256 columns each) keeps
-    // one of each: the softmax frees S as soon as its row is in registers, so
-    // the next QK^T still overlaps the exponentials.
-    static constexpr int NBUF = (D == 64) ? 1 : 2;
+    static_assert(THREADS != 256 || (REG_SOFTMAX + REG_OTHER) * 128 * CTAS_PER_SM == 65536, "register split");
+    static constexpr int BN = (D == 64) ? 128 : 64;      // keys per tile
+    // S and P buffers in TMEM.  D=64/128 (two CTAs per SM, 256 columns each)
+    // keep one of each (D=64: S 128 + O 64 + P 64; D=128 with 64-key tiles:
+    // S 64 + O 128 + P 32): the softmax frees S as soon as its row is in
+    // registers, so the next QK^T still overlaps the exponentials.  D=256
+    // double-buffers both.
+    static constexpr int NBUF = (D <= 128) ? 1 : 2;
     // K/V ring depths: K is consumed a whole softmax earlier than V, so it gets
-    // the deeper ring where shared memory allows
-    static constexpr int KST = 3;
+    // the deeper ring where shared memory allows (two D=128 CTAs per SM leave
+    // room for two of each)
+    static constexpr int KST = (D == 128) ? 2 : 3;
     static constexpr int VST = 2;
     static constexpr int STAGES = KST > VST ? KST : VST;  // barrier array size
     static constexpr uint32_t Q_BYTES = NCH * BM * 128;
