@@ -52,7 +52,7 @@ def _load():
             lib.oracle_f16_to_double.restype = f64
             lib.oracle_decode.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i64, i64,
                                           i32, i32, i32, i32, i32, f64, f64,
-                                          i32, P, P, P, P, i32]
+                                          i32, P, P, P, P, i32, i32]
             lib.oracle_decode.restype = i32
             lib.oracle_prefill.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, f64, f64,
                                            i32, P, P, P, P, i32]
@@ -126,7 +126,8 @@ def decode(case, rows=None, n_threads: int = 0):
                            int(case.max_pages or 0), int(case.cap), n_pages,
                            case.batch, case.n_heads, case.n_kv_heads, case.head_dim,
                            int(case.window), float(case.softcap), float(case.scale),
-                           n_rows, _ptr(rb), _ptr(rh), _ptr(out), _ptr(lse), int(n_threads))
+                           n_rows, _ptr(rb), _ptr(rh), _ptr(out), _ptr(lse), int(n_threads),
+                           int(getattr(case, "ring", 0) or 0))
     if rc != 0:
         raise ValueError("oracle_decode rejected its arguments")
     return out, lse

@@ -149,6 +149,11 @@ static double oracle_cache_value(const void* cache, const uint16_t* scales, int 
  * Decode: one new query per sequence, at position kv_len[b]-1.
  * rows: n_rows (b, h) pairs to evaluate (rows_b/rows_h), or n_rows < 0 for all
  * B*Hq in (b, h) row-major order.  out: [n][D], lse: [n].
+ * ring > 0: the cache is a ring of `ring` slots per sequence (doppler run.js,
+ * runLayerAttentionGPU: a SlidingWindowKVCache selects kvLayout 'ring' and
+ * kvStart = totalSeqLen - kvLen): logical token t lives in slot t % ring of the
+ * contiguous [B][ring][Hkv][D] layout, kv_len is the logical length (not
+ * clamped), and the kept keys are the last min(kv_len, ring, window) tokens.
  * Returns 0, or -1 on an invalid argument.
  */
 int oracle_decode(const uint16_t* q, const void* k, const void* v, int kv_int8,
@@ -157,10 +162,11 @@ int oracle_decode(const uint16_t* q, const void* k, const void* v, int kv_int8,
                   int page_size, int max_pages, long cap, long n_pages,
                   int B, int Hq, int Hkv, int D, int window, double softcap, double scale,
                   int n_rows, const int32_t* rows_b, const int32_t* rows_h,
-                  double* out, double* lse, int n_threads)
+                  double* out, double* lse, int n_threads, int ring)
 {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return -1;
     if (page_table && page_size <= 0) return -1;
+    if (ring > 0 && (page_table || ring != cap)) return -1;
     int G = Hq / Hkv;
     long n = n_rows < 0 ? (long)B * Hq : n_rows;
 #ifdef _OPENMP
@@ -173,8 +179,29 @@ int oracle_decode(const uint16_t* q, const void* k, const void* v, int kv_int8,
         int g = h / G;
         long L = kv_len[b];
         long cap_b = page_table ? (long)max_pages * page_size : cap;
-        if (L > cap_b) L = cap_b;
         if (L < 0) L = 0;
+        if (ring > 0) {
+            /* the kept logical keys t0 .. L-1, gathered from their slots t % ring */
+            long keep = L < ring ? L : ring;
+            if (window > 0 && window < keep) keep = window;
+            long t0 = L - keep;
+            double* qd = (double*)malloc(sizeof(double) * D);
+            double* Kd = (double*)malloc(sizeof(double) * (size_t)(keep > 0 ? keep : 1) * D);
+            double* Vd = (double*)malloc(sizeof(double) * (size_t)(keep > 0 ? keep : 1) * D);
+            for (int d = 0; d < D; ++d)
+                qd[d] = oracle_f16_to_double(q[((long)b * Hq + h) * D + d]);
+            for (long t = 0; t < keep; ++t)
+                for (int d = 0; d < D; ++d) {
+                    long slot = (t0 + t) % ring;
+                    Kd[t * D + d] = oracle_cache_value(k, k_scales, kv_int8, NULL, 0, 0, cap, 0, b, slot, g, d, Hkv, D);
+                    Vd[t * D + d] = oracle_cache_value(v, v_scales, kv_int8, NULL, 0, 0, cap, 0, b, slot, g, d, Hkv, D);
+                }
+            /* every gathered key is kept: the query is the last of them */
+            oracle_attend(qd, Kd, Vd, keep, D, keep - 1, 1, 0, softcap, scale, out + r * D, lse + r);
+            free(qd); free(Kd); free(Vd);
+            continue;
+        }
+        if (L > cap_b) L = cap_b;
         double* qd = (double*)malloc(sizeof(double) * D);
         double* Kd = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);
         double* Vd = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);

@@ -37,6 +37,7 @@ __all__ = [
     "make_decode_case",
     "make_prefill_case",
     "paged_from_contiguous",
+    "ring_from_contiguous",
     "ChunkCase",
     "make_chunked_case",
     "WORKLOADS",
@@ -121,6 +122,7 @@ class DecodeCase:
     softcap: float = 0.0
     scale: float = 0.0
     lens: list = field(default_factory=list)
+    ring: int = 0          # > 0: k/v [B, ring, Hkv, D] hold logical token t in slot t % ring
 
     @property
     def paged(self) -> bool:
@@ -268,6 +270,33 @@ def make_decode_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int,
                       k_scales=ks, v_scales=vs, page_table=pt.to(device), page_size=P,
                       max_pages=max_pages, window=window, softcap=softcap,
                       scale=float(scale), lens=lens)
+
+
+def ring_from_contiguous(case: DecodeCase, ring: int) -> DecodeCase:
+    """The same logical tokens in a ring cache of ``ring`` slots per sequence:
+    slot t % ring holds the newest token t that maps to it (older ones are
+    overwritten, as a sliding-window cache does).  The contiguous case must hold
+    every logical token (cap >= max kv_len)."""
+    assert not case.paged and not case.ring
+    B = case.batch
+    dev = case.k.device
+    kr = torch.zeros((B, ring) + tuple(case.k.shape[2:]), dtype=case.k.dtype, device=dev)
+    vr = torch.zeros_like(kr)
+    ksr = vsr = None
+    if case.int8:
+        ksr = torch.zeros((B, case.n_kv_heads, ring), dtype=torch.float16, device=dev)
+        vsr = torch.zeros_like(ksr)
+    for b in range(B):
+        L = int(case.lens[b])
+        for t in range(max(0, L - ring), L):
+            kr[b, t % ring] = case.k[b, t]
+            vr[b, t % ring] = case.v[b, t]
+            if case.int8:
+                ksr[b, :, t % ring] = case.k_scales[b, :, t]
+                vsr[b, :, t % ring] = case.v_scales[b, :, t]
+    kw = dict(case.__dict__)
+    kw.update(k=kr, v=vr, k_scales=ksr, v_scales=vsr, cap=ring, ring=ring)
+    return DecodeCase(**kw)
 
 
 def paged_from_contiguous(case: DecodeCase, page_size: int, seed: int,

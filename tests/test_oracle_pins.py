@@ -469,3 +469,37 @@ def test_empty_chunks_are_skipped():
                                                        page_size=4), rows=[(r, h) for r in range(3)
                                                                           for h in range(2)])
     assert np.array_equal(got, ref)
+
+
+# ---- ring (sliding-window) cache ---------------------------------------------
+
+@pytest.mark.parametrize("int8", [False, True])
+@pytest.mark.parametrize("ring,window", [(16, 0), (32, 0), (32, 20), (48, 100)])
+def test_ring_equals_contiguous_with_its_window(int8, ring, window):
+    # a ring of R slots keeps the last min(L, R, W) logical tokens: the same as a
+    # contiguous cache of every token with the window min(W, R)
+    lens = [5, 16, 47, 100]
+    cc = si.make_decode_case(4, 4, 2, 32, lens, seed=41, int8=int8, cap=104, window=window)
+    rc = si.ring_from_contiguous(cc, ring)
+    w_eff = ring if window <= 0 else min(window, ring)
+    cc.window = w_eff
+    a, la = oracle.decode(cc)
+    b, lb = oracle.decode(rc)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+def test_ring_matches_brute_force():
+    cc = si.make_decode_case(2, 2, 1, 16, [70, 9], seed=43, cap=72)
+    rc = si.ring_from_contiguous(cc, 32)
+    got, lse = oracle.decode(rc)
+    q = cc.q.double().numpy()
+    for b, L in enumerate([70, 9]):
+        keep = min(L, 32)
+        ts = list(range(L - keep, L))
+        K = np.stack([rc.k[b, t % 32, 0].double().numpy() for t in ts])
+        V = np.stack([rc.v[b, t % 32, 0].double().numpy() for t in ts])
+        for h in range(2):
+            s = rc.scale * K @ q[b, h]
+            p = scipy.special.softmax(s)
+            np.testing.assert_allclose(got[b * 2 + h], p @ V, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[b * 2 + h], scipy.special.logsumexp(s), rtol=0, atol=1e-12)
