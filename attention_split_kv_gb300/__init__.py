@@ -19,7 +19,7 @@ __all__ = [
     "ATTN_KV_F16", "ATTN_KV_INT8", "AttnError", "AttnLibraryMissing",
     "lib_path", "load", "build", "exported_symbols",
     "attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-    "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate", "attn_device_status",
+    "attn_decode_ring", "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate", "attn_device_status",
     "decode", "prefill", "prefill_paged",
 ]
 
@@ -34,7 +34,7 @@ _lib = None
 
 # every entry point include/attn.h declares
 exported_symbols = ("attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-                    "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate",
+                    "attn_decode_ring", "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate",
                     "attn_device_status")
 
 
@@ -72,6 +72,8 @@ def load():
     lib.attn_decode_workspace_size.restype = SZ
     lib.attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, I, I, I, I, I, F, F, I, P, P, P, SZ, P]
     lib.attn_decode.restype = I
+    lib.attn_decode_ring.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, F, F, I, P, P, P, SZ, P]
+    lib.attn_decode_ring.restype = I
     lib.attn_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, I, I, I, I, I, F, F, I, P, P, P]
     lib.attn_decode_noalloc.restype = I
     lib.attn_prefill.argtypes = [P, P, P, I, I, I, I, I, I, F, F, P, P, P]
@@ -131,6 +133,16 @@ def attn_decode(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_pe
                               int(workspace_bytes), _stream(stream)))
 
 
+def attn_decode_ring(q, k_ring, v_ring, seq_len, ring_size, k_scales, v_scales, kv_dtype, batch, n_heads,
+                     n_kv_heads, head_dim, window, softcap, scale, split_keys, out, lse_out, workspace,
+                     workspace_bytes, stream=None) -> None:
+    _check(load().attn_decode_ring(_ptr(q), _ptr(k_ring), _ptr(v_ring), _ptr(seq_len), int(ring_size),
+                                   _ptr(k_scales), _ptr(v_scales), int(kv_dtype), int(batch), int(n_heads),
+                                   int(n_kv_heads), int(head_dim), int(window), float(softcap), float(scale),
+                                   int(split_keys), _ptr(out), _ptr(lse_out), _ptr(workspace),
+                                   int(workspace_bytes), _stream(stream)))
+
+
 def attn_decode_noalloc(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages,
                         max_kv, k_scales, v_scales, kv_dtype, batch, n_heads, n_kv_heads, head_dim, window,
                         softcap, scale, split_keys, out, lse_out, stream=None) -> None:
@@ -169,15 +181,17 @@ def attn_device_status(stream=None) -> int:
 # ---------------------------------------------------------------- conveniences
 def decode(case, out=None, lse_out=None, workspace=None, split_keys: int = 0, max_kv: Optional[int] = None,
            stream=None):
-    """attn_decode on a DecodeCase-like object (tensors already on the GPU).
+    """attn_decode on a DecodeCase-like object (tensors already on the GPU);
+    attn_decode_ring when the case holds a ring cache (``case.ring > 0``).
 
     Allocates ``out`` (and the workspace) with torch when not given.
     """
     import torch
     dev = case.q.device
     B, Hq, Hkv, D = case.batch, case.n_heads, case.n_kv_heads, case.head_dim
+    ring = int(getattr(case, "ring", 0) or 0)
     if max_kv is None:
-        max_kv = case.cap
+        max_kv = ring if ring else case.cap
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float16, device=dev)
     ws_bytes = attn_decode_workspace_size(B, Hq, Hkv, D, max_kv, split_keys)
@@ -185,6 +199,11 @@ def decode(case, out=None, lse_out=None, workspace=None, split_keys: int = 0, ma
         raise AttnError(ATTN_EINVAL, "invalid sizes for the decode workspace")
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if ring:
+        attn_decode_ring(case.q, case.k, case.v, case.kv_len, ring, case.k_scales, case.v_scales,
+                         ATTN_KV_INT8 if case.int8 else ATTN_KV_F16, B, Hq, Hkv, D, case.window, case.softcap,
+                         case.scale, split_keys, out, lse_out, workspace, workspace.numel(), stream)
+        return out
     attn_decode(case.q, case.k, case.v, case.kv_len, case.page_table, case.page_size, case.max_pages,
                 case.n_pages, max_kv, case.k_scales, case.v_scales,
                 ATTN_KV_INT8 if case.int8 else ATTN_KV_F16, B, Hq, Hkv, D, case.window, case.softcap,

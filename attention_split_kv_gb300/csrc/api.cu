@@ -176,11 +176,13 @@ size_t attn_decode_workspace_size(int batch, int n_heads, int n_kv_heads, int he
     return plan.bytes;
 }
 
-attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
-                        const int32_t* page_table, int page_size, int max_pages_per_seq, int n_pages, int max_kv,
-                        const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype, int batch, int n_heads,
-                        int n_kv_heads, int head_dim, int window, float softcap, float scale, int split_keys,
-                        void* out, float* lse_out, void* workspace, size_t workspace_bytes, void* stream) {
+// attn_decode and attn_decode_ring: ring > 0 selects the ring cache
+static attn_status decode_entry(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
+                                const int32_t* page_table, int page_size, int max_pages_per_seq, int n_pages,
+                                int max_kv, const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
+                                int batch, int n_heads, int n_kv_heads, int head_dim, int window, float softcap,
+                                float scale, int split_keys, void* out, float* lse_out, void* workspace,
+                                size_t workspace_bytes, void* stream, int ring) {
     if (!q || !k_cache || !v_cache || !kv_len || !out)
         return set_error(ATTN_EINVAL, "attn_decode: q, k_cache, v_cache, kv_len and out must be non-null");
     if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0)
@@ -243,7 +245,9 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
     L.Hq = n_heads;
     L.Hkv = n_kv_heads;
     L.D = head_dim;
-    L.window = window;
+    // a ring keeps at most `ring` logical tokens: the window is never wider
+    L.window = ring > 0 ? ((window > 0 && window < ring) ? window : ring) : window;
+    L.ring = ring;
     L.softcap = softcap;
     L.scale = scale;
     L.split_keys = split_keys;
@@ -254,6 +258,29 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
     L.err_word = err;
     L.stream = static_cast<cudaStream_t>(stream);
     return launch_decode(L, plan);
+}
+
+attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
+                        const int32_t* page_table, int page_size, int max_pages_per_seq, int n_pages, int max_kv,
+                        const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype, int batch, int n_heads,
+                        int n_kv_heads, int head_dim, int window, float softcap, float scale, int split_keys,
+                        void* out, float* lse_out, void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_entry(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages, max_kv,
+                        k_scales, v_scales, kv_dtype, batch, n_heads, n_kv_heads, head_dim, window, softcap, scale,
+                        split_keys, out, lse_out, workspace, workspace_bytes, stream, 0);
+}
+
+attn_status attn_decode_ring(const void* q, const void* k_ring, const void* v_ring, const int32_t* seq_len,
+                             int ring_size, const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
+                             int batch, int n_heads, int n_kv_heads, int head_dim, int window, float softcap,
+                             float scale, int split_keys, void* out, float* lse_out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    if (ring_size < 16 || ring_size % 16 != 0)
+        return set_error(ATTN_EUNSUPPORTED, "attn_decode_ring: ring_size %d must be a positive multiple of 16",
+                         ring_size);
+    return decode_entry(q, k_ring, v_ring, seq_len, nullptr, 0, 0, 0, ring_size, k_scales, v_scales, kv_dtype,
+                        batch, n_heads, n_kv_heads, head_dim, window, softcap, scale, split_keys, out, lse_out,
+                        workspace, workspace_bytes, stream, ring_size);
 }
 
 attn_status attn_prefill(const void* q, const void* k, const void* v, int seq_len, int n_heads, int n_kv_heads,

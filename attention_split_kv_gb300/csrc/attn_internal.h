@@ -78,6 +78,7 @@ struct DecodeLaunch {
     int B, Hq, Hkv, D, window;
     float softcap, scale;
     int split_keys;
+    int ring = 0;           // > 0: contiguous ring of `ring` slots, logical token t in slot t % ring
     void* out;
     float* lse;
     void* workspace;

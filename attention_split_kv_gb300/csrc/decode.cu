@@ -96,6 +96,7 @@ struct DecArgs {
     float* ws_fix_lse;
     float* ws_fix_o;
     int B, Hq, Hkv, G, HG, U, n_hb, nh_box, split, cap_eff, window, P, R, max_pages, n_pages, paged;
+    int ring;          // > 0: contiguous ring cache, logical token t in row t % ring
     float qscale;      // multiplies q: scale*log2e (no cap) or scale/c (cap)
     float cap_log2;    // c*log2e, 0 when the cap is off
     int* err;
@@ -325,6 +326,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                         page = 0;
                     }
                     row = (A.P >= T) ? (t0 % A.P) : 0;
+                } else if (A.ring > 0) {
+                    row = t0 % A.ring;   // 16-token tiles never wrap: ring % 16 == 0
                 }
                 if (lane == 0) {
                     tma_load_4d(sb + r * box_kv, &tm_k, full_bar(slot), 0, g0, row, page);
@@ -774,7 +777,9 @@ DecArgs make_dec_args(const DecodeLaunch& L, const DecodePlan& plan, int R) {
     a.n_hb = plan.n_hb;
     a.nh_box = plan.nh_box;
     a.split = plan.split;
-    a.cap_eff = cap_layout < L.max_kv ? cap_layout : L.max_kv;
+    // a ring holds the newest `ring` tokens of sequences of any length: no clamp
+    a.cap_eff = L.ring > 0 ? (1 << 30) : (cap_layout < L.max_kv ? cap_layout : L.max_kv);
+    a.ring = L.ring;
     a.window = L.window;
     a.P = paged ? L.page_size : 0;
     a.R = R;

@@ -264,7 +264,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 mbar_arrive_expect_tx(bar(b_full + slot), nbox * NCH * BOXB);
                 for (int bx = 0; bx < nbox; ++bx) {
                     const int tk = t0 + bx * 16;
-                    int page = c.b, row = tk;
+                    int page = c.b, row = A.ring > 0 ? tk % A.ring : tk;   // ring: slot t % ring (ring % 16 == 0)
                     if (A.paged) {
                         page = __ldg(&A.page_table[(size_t)c.b * A.max_pages + tk / A.P]);
                         if (page < 0 || page >= A.n_pages) {

@@ -118,6 +118,42 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_ring -- attn_decode over a ring (rolling-buffer) KV cache, the
+ * layout a sliding-window model keeps: each sequence owns ring_size slots and
+ * token t is written to slot t % ring_size, overwriting token t - ring_size.
+ * (Sliding-window attention, rolling buffer cache; the window of W tokens
+ * needs no more than W slots.)
+ *
+ *  k_ring,     device, [B, ring_size, Hkv, D] f16 or int8 codes; token t of
+ *  v_ring        sequence b at [b, t % ring_size].
+ *  seq_len     device, int32 [B]: L_b, the LOGICAL number of tokens the
+ *                sequence has seen, including the new one (any value; not
+ *                clamped to ring_size).  The query's position is L_b - 1.
+ *                L_b <= 0 yields a zero output row and lse = -inf.
+ *  ring_size   slots per sequence: a positive multiple of 16, so no 16-token
+ *                tile wraps round the ring.  ATTN_EUNSUPPORTED otherwise.
+ *  k_scales,   int8 caches only: [B, Hkv, ring_size], slot-indexed like the
+ *  v_scales      codes.
+ *  window      W > 0 keeps the W most recent tokens; the ring itself keeps
+ *                at most ring_size, so the kept keys are the last
+ *                min(L_b, ring_size, W or ring_size) tokens.
+ *  workspace   >= attn_decode_workspace_size(B, Hq, Hkv, D, ring_size,
+ *                split_keys).
+ *  The other arguments are those of attn_decode.  Slots that hold no kept
+ *  token (not yet written, or older than the window) are never used for the
+ *  result, whatever they contain.  A ring whose slots hold the same values as
+ *  a contiguous cache's last kept tokens gives the result of attn_decode on
+ *  that cache with the window min(ring_size, W), up to fp32 rounding order.
+ */
+attn_status attn_decode_ring(const void* q, const void* k_ring, const void* v_ring,
+                             const int32_t* seq_len, int ring_size,
+                             const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
+                             int batch, int n_heads, int n_kv_heads, int head_dim,
+                             int window, float softcap, float scale, int split_keys,
+                             void* out, float* lse_out,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
  * memory, so cannot supply a workspace: for example a plugin running inside
  * an engine that owns all device memory and offers it no allocator, or a

@@ -275,17 +275,24 @@ def make_decode_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int,
 def ring_from_contiguous(case: DecodeCase, ring: int) -> DecodeCase:
     """The same logical tokens in a ring cache of ``ring`` slots per sequence:
     slot t % ring holds the newest token t that maps to it (older ones are
-    overwritten, as a sliding-window cache does).  The contiguous case must hold
-    every logical token (cap >= max kv_len)."""
+    overwritten, as a sliding-window cache does).  Slots no token has reached
+    yet hold seeded filler values (finite, larger than the real ones), which no
+    result may depend on.  The contiguous case must hold every logical token
+    (cap >= max kv_len)."""
     assert not case.paged and not case.ring
     B = case.batch
     dev = case.k.device
-    kr = torch.zeros((B, ring) + tuple(case.k.shape[2:]), dtype=case.k.dtype, device=dev)
-    vr = torch.zeros_like(kr)
-    ksr = vsr = None
+    shape = (B, ring) + tuple(case.k.shape[2:])
+    filler = f16_normal(shape, 7919 + ring, dev) * 4
     if case.int8:
-        ksr = torch.zeros((B, case.n_kv_heads, ring), dtype=torch.float16, device=dev)
-        vsr = torch.zeros_like(ksr)
+        kr = filler.clamp(-127, 127).to(torch.int8)
+        vr = kr.flip(-1).contiguous()
+        ksr = (f16_normal((B, case.n_kv_heads, ring), 7927 + ring, dev).abs() + 0.5).to(torch.float16)
+        vsr = ksr.flip(-1).contiguous()
+    else:
+        kr = filler.to(case.k.dtype)
+        vr = kr.flip(-1).contiguous()
+        ksr = vsr = None
     for b in range(B):
         L = int(case.lens[b])
         for t in range(max(0, L - ring), L):

@@ -99,6 +99,33 @@ def test_decode_rejects_bad_arguments_on_host(lib, kw, status):
     assert attn.attn_last_error()
 
 
+def _decode_ring(**kw):
+    args = dict(q=FAKE, k_ring=FAKE, v_ring=FAKE, seq_len=FAKE, ring_size=64, k_scales=None, v_scales=None,
+                kv_dtype=attn.ATTN_KV_F16, batch=1, n_heads=4, n_kv_heads=2, head_dim=64, window=0,
+                softcap=0.0, scale=0.125, split_keys=0, out=FAKE, lse_out=None, workspace=FAKE,
+                workspace_bytes=1 << 30, stream=0)
+    args.update(kw)
+    return attn.load().attn_decode_ring(*[args[k] for k in (
+        "q", "k_ring", "v_ring", "seq_len", "ring_size", "k_scales", "v_scales", "kv_dtype", "batch",
+        "n_heads", "n_kv_heads", "head_dim", "window", "softcap", "scale", "split_keys", "out", "lse_out",
+        "workspace", "workspace_bytes", "stream")])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(ring_size=0), attn.ATTN_EUNSUPPORTED),
+    (dict(ring_size=40), attn.ATTN_EUNSUPPORTED),        # not a multiple of 16
+    (dict(ring_size=-32), attn.ATTN_EUNSUPPORTED),
+    (dict(seq_len=None), attn.ATTN_EINVAL),
+    (dict(head_dim=96), attn.ATTN_EUNSUPPORTED),
+    (dict(kv_dtype=attn.ATTN_KV_INT8), attn.ATTN_EINVAL),  # scales missing
+    (dict(window=-1), attn.ATTN_EINVAL),
+    (dict(workspace_bytes=16), attn.ATTN_EINVAL),
+])
+def test_decode_ring_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _decode_ring(**kw) == status
+    assert attn.attn_last_error()
+
+
 def _prefill(**kw):
     args = dict(q=FAKE, k=FAKE, v=FAKE, seq_len=128, n_heads=4, n_kv_heads=2, head_dim=64, causal=1,
                 window=0, softcap=0.0, scale=0.125, out=FAKE, lse_out=None, stream=0)
