@@ -172,8 +172,14 @@ struct PrefillArgs {
     const int32_t* kv_len;
     const int32_t* page_table;
     int P, log2P, max_pages, n_pages, box_rows;
+    int B, max_qt;     // sequences, query tiles of the longest chunk
+    int lpt;           // 1: a 1-D grid walks (sequence, query tile) pairs longest first
     int total_q;       // rows of q/out (S for contiguous prefill)
 };
+
+// Chunks with at most this many (sequence, query tile) pairs are launched
+// longest first: every CTA ranks all pairs by their key tiles.
+constexpr int kLptMaxPairs = 128;
 
 template <int D, int MODE, bool PAGED>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, PrefillCfg<D>::CTAS_PER_SM)
@@ -200,30 +206,71 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // Geometry.  Queries i in [0, n_q) of one sequence sit at positions pos0 + i
     // over keys [0, L); contiguous prefill has one sequence of S tokens with
     // positions 0 .. S-1, a paged chunk the last n_q of its sequence's tokens.
-    int n_q = args.S, L = args.S, pos0 = 0, q_base = 0, b = 0;
+    const int W = args.window;
+    // key tiles [jt0, jt0 + count) kept by queries q0 .. q_last at positions pos0 + i over L keys
+    auto key_tiles = [&](int L_, int pos0_, int q0_, int q_last_, int& jt0_) {
+        int hi_ = args.causal ? min(L_, pos0_ + q_last_ + 1) : L_;
+        if (!args.causal && W > 0) hi_ = min(L_, q_last_ + W);
+        const int lo_ = W > 0 ? max(0, pos0_ + q0_ - W + 1) : 0;
+        jt0_ = lo_ / BN;
+        return hi_ > lo_ ? (hi_ + BN - 1) / BN - jt0_ : 0;
+    };
+    int n_q = args.S, L = args.S, pos0 = 0, q_base = 0, b = 0, qt = 0, h = blockIdx.y;
     if constexpr (PAGED) {
-        b = blockIdx.z;
-        q_base = args.q_start[b];
-        n_q = args.q_start[b + 1] - q_base;
-        const int kvl = args.kv_len[b];
-        L = min(max(kvl, 0), args.max_pages * args.P);
-        pos0 = kvl - n_q;
+        auto chunk_of = [&](int bb, int& qs, int& nq, int& Lb, int& p0) {
+            qs = args.q_start[bb];
+            nq = args.q_start[bb + 1] - qs;
+            const int kvl = args.kv_len[bb];
+            Lb = min(max(kvl, 0), args.max_pages * args.P);
+            p0 = kvl - nq;
+        };
+        if (args.lpt) {
+            // longest first across sequences: CTA x takes head x % Hq of the
+            // (x / Hq)-th (sequence, query tile) pair in decreasing order of key
+            // tiles (ties by index), so the last wave holds the shortest CTAs.
+            // The scratch sits where Q lands, before any copy is issued.
+            int* wk = reinterpret_cast<int*>(smem + C::OFF_Q);
+            int* sel = wk + kLptMaxPairs;
+            const int n_pairs = args.B * args.max_qt;
+            if (threadIdx.x < n_pairs) {
+                const int bb = threadIdx.x / args.max_qt, t = threadIdx.x % args.max_qt;
+                int qs, nq, Lb, p0, j0, w = -1;   // -1: no queries, ranked last
+                chunk_of(bb, qs, nq, Lb, p0);
+                if (t * BM < nq) w = key_tiles(Lb, p0, t * BM, min(t * BM + BM - 1, nq - 1), j0);
+                wk[threadIdx.x] = w;
+            }
+            __syncthreads();
+            const int want = static_cast<int>(blockIdx.x) / args.Hq;
+            if (threadIdx.x < n_pairs) {
+                const int me = wk[threadIdx.x];
+                int rank = 0;
+                for (int j = 0; j < n_pairs; ++j) {
+                    const int o = wk[j];
+                    rank += (o > me || (o == me && j < static_cast<int>(threadIdx.x))) ? 1 : 0;
+                }
+                if (rank == want) *sel = threadIdx.x;   // ranks are a permutation: one writer
+            }
+            __syncthreads();
+            const int pair = *sel;
+            b = pair / args.max_qt;
+            qt = pair % args.max_qt;
+            h = static_cast<int>(blockIdx.x) % args.Hq;
+        } else {
+            b = blockIdx.z;
+            qt = static_cast<int>(gridDim.x - 1 - blockIdx.x);
+        }
+        chunk_of(b, q_base, n_q, L, pos0);
     }
     const int n_qt = (n_q + BM - 1) / BM;
     // causal tiles late in the sequence carry the most keys: launch them first
-    const int qt = PAGED ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
-                         : (args.causal ? (n_qt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
+    if constexpr (!PAGED)
+        qt = args.causal ? (n_qt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
     if (PAGED && qt >= n_qt) return;   // a shorter chunk: no queries for this CTA
-    const int h = blockIdx.y;
     const int g = h / (args.Hq / args.Hkv);
     const int q0 = qt * BM;
     const int q_last = min(q0 + BM - 1, n_q - 1);
-    const int W = args.window;
-    int hi = args.causal ? min(L, pos0 + q_last + 1) : L;
-    if (!args.causal && W > 0) hi = min(L, q_last + W);
-    const int lo = W > 0 ? max(0, pos0 + q0 - W + 1) : 0;
-    const int jt0 = lo / BN;
-    const int n_tiles = hi > lo ? (hi + BN - 1) / BN - jt0 : 0;
+    int jt0;
+    const int n_tiles = key_tiles(L, pos0, q0, q_last, jt0);
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_QFULL), 1);
@@ -273,6 +320,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         tma_load_3d(sbase + C::OFF_Q + c * (BM * 128), &tm_q, bar(B_QFULL), c * 64, h, q_base + q0);
                 }
                 int issued = 0;
+                // paged: one box of R rows per page (or one box inside a page).  The
+                // page ids of tile j+1 are loaded right after tile j's copies are
+                // issued, so their latency hides behind the wait for a free stage.
+                constexpr int MAXB = PAGED ? BN / 8 : 1;   // boxes per tile (pages >= 8 tokens)
+                const int R = PAGED ? args.box_rows : BN;
+                int pg[MAXB];
+                auto fetch_pages = [&](int j) {
+                    const int key0 = (jt0 + j) * BN;
+#pragma unroll
+                    for (int i = 0; i < MAXB; ++i) {
+                        const int kk = key0 + i * R;
+                        pg[i] = 0;
+                        if (i * R < BN && j < n_tiles && kk < L)
+                            pg[i] = __ldg(&args.page_table[(size_t)b * args.max_pages + (kk >> args.log2P)]);
+                    }
+                };
+                if constexpr (PAGED) fetch_pages(0);
                 for (int j = 0; j < n_tiles; ++j) {
                     const int st = j % NST;
                     if (j >= NST &&
@@ -281,16 +345,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const int key0 = (jt0 + j) * BN;
                     mbar_arrive_expect_tx(bar(b_full + st), C::KV_BYTES);
                     if constexpr (PAGED) {
-                        // one box of box_rows rows per page (or one box inside a page);
                         // boxes past the cached keys get the page coordinate n_pages, past
                         // the pool, so the copy fills zeros instead of reading anything
-                        const int R = args.box_rows;
-                        for (int i = 0; i * R < BN; ++i) {
+#pragma unroll
+                        for (int i = 0; i < MAXB; ++i) {
+                            if (i * R >= BN) break;
                             const int kk = key0 + i * R;
                             int page = args.n_pages, row = 0;
                             if (kk < L) {
-                                const int pid = __ldg(&args.page_table[(size_t)b * args.max_pages + (kk >> args.log2P)]);
-                                if (pid >= 0 && pid < args.n_pages) page = pid;
+                                if (pg[i] >= 0 && pg[i] < args.n_pages) page = pg[i];
                                 else atomicExch(args.err, kErrBadPage);   // never read: reported
                                 row = kk & (args.P - 1);
                             }
@@ -298,6 +361,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                 tma_load_4d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK + i * R * 128, tm,
                                             bar(b_full + st), c * 64, g, row, page);
                         }
+                        fetch_pages(j + 1);
                     } else {
                         for (int c = 0; c < NCH; ++c)
                             tma_load_3d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK, tm, bar(b_full + st), c * 64,
@@ -641,7 +705,12 @@ attn_status launch_prefill_dm(const PrefillLaunch& L) {
     a.n_pages = L.n_pages;
     a.box_rows = box_rows;
     a.total_q = PAGED ? L.total_q : L.S;
-    const dim3 grid = PAGED ? dim3((L.max_q + BM - 1) / BM, L.Hq, L.B) : dim3((L.S + BM - 1) / BM, L.Hq);
+    a.B = L.B;
+    a.max_qt = PAGED ? (L.max_q + BM - 1) / BM : 0;
+    const int n_pairs = L.B * a.max_qt;
+    a.lpt = PAGED && n_pairs <= kLptMaxPairs;
+    const dim3 grid = !PAGED ? dim3((L.S + BM - 1) / BM, L.Hq)
+                      : a.lpt ? dim3(n_pairs * L.Hq) : dim3(a.max_qt, L.Hq, L.B);
     prefill_tc_kernel<D, MODE, PAGED><<<grid, C::THREADS, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));

@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
 }
 METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
 WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode",
-                  "chunked_prefill_paged"]
+                  "chunked_prefill_paged", "ring_window_decode"]
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -108,8 +108,11 @@ def decode_bytes(case):
     per_tok = case.n_kv_heads * case.head_dim * esz * 2 + (case.n_kv_heads * 2 * 2 if case.int8 else 0)
     kv = 0
     pages = 0
+    ring = getattr(case, "ring", 0) or 0
     for L in case.lens:
         Le = min(L, case.window) if case.window > 0 else L
+        if ring:
+            Le = min(Le, ring)
         kv += Le * per_tok
         if case.paged:
             pages += (L + case.page_size - 1) // case.page_size
@@ -129,7 +132,8 @@ def workload_config(case):
                 "softcap": case.softcap}
     return {"global_batch": case.batch, "n_heads": case.n_heads, "n_kv_heads": case.n_kv_heads,
             "head_dim": case.head_dim, "kv_len_min": min(case.lens), "kv_len_max": max(case.lens),
-            "kv_dtype": "int8" if case.int8 else "f16", "page_size": case.page_size}
+            "kv_dtype": "int8" if case.int8 else "f16", "page_size": case.page_size,
+            **({"ring": case.ring} if getattr(case, "ring", 0) else {})}
 
 
 # ---------------------------------------------------------------- clocks

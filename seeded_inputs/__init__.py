@@ -213,13 +213,16 @@ def make_decode_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int,
                      lens, seed: int, *, cap: Optional[int] = None, int8: bool = False,
                      page_size: int = 0, n_pages: Optional[int] = None,
                      window: int = 0, softcap: float = 0.0, scale: Optional[float] = None,
-                     device: str = "cpu") -> DecodeCase:
+                     ring: int = 0, device: str = "cpu") -> DecodeCase:
     """Build a decode case.
 
     ``lens`` is a list of per-sequence KV lengths, or a (lo, hi) tuple for
     seeded uniform lengths.  With ``page_size > 0`` the cache is paged: a pool of
     ``n_pages`` pages (default: just enough) filled with N(0,1) values, and a
-    seeded permutation assigning pages to sequences.
+    seeded permutation assigning pages to sequences.  With ``ring > 0`` the cache
+    is a ring of ``ring`` slots per sequence, drawn directly (every slot holds
+    N(0,1) values, as a ring does once its sequence has passed ``ring`` tokens);
+    ``lens`` are then logical lengths and may exceed ``ring``.
     """
     if isinstance(lens, tuple):
         lens = _lengths(batch, lens[0], lens[1], seed)
@@ -229,6 +232,9 @@ def make_decode_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int,
         scale = 1.0 / math.sqrt(head_dim)
     q = f16_normal((batch, n_heads, head_dim), seed * 1000 + 1, device)
     kv_len = torch.tensor(lens, dtype=torch.int32, device=device)
+    if ring > 0:
+        assert page_size <= 0
+        cap = ring
     if page_size <= 0:
         if cap is None:
             cap = max(max(lens), 1)
@@ -244,7 +250,7 @@ def make_decode_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int,
         return DecodeCase(q=q, k=k, v=v, kv_len=kv_len, batch=batch, n_heads=n_heads,
                           n_kv_heads=n_kv_heads, head_dim=head_dim, cap=cap, int8=int8,
                           k_scales=ks, v_scales=vs, window=window, softcap=softcap,
-                          scale=float(scale), lens=lens)
+                          scale=float(scale), lens=lens, ring=ring)
     P = page_size
     need = [(L + P - 1) // P for L in lens]
     max_pages = max(max(need), 1)
@@ -419,6 +425,11 @@ WORKLOADS = {
                              window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
     # chunked prefill over a paged cache: 8 sequences append 512-token chunks to
     # 512..7680 cached tokens (16-token pages), the GQA shape of the paged decode
+    # sliding-window decode over a 4096-slot ring cache: 32 sequences at logical
+    # lengths 4K..64K (each keeps its newest 4096 tokens), the paged decode's GQA shape
+    "ring_window_decode": dict(kind="decode", seed=7, batch=32, n_heads=32, n_kv_heads=8, head_dim=128,
+                               lens=(4096, 65536), int8=False, page_size=0, ring=4096, window=0,
+                               softcap=0.0, scale=1.0 / math.sqrt(128.0)),
     "chunked_prefill_paged": dict(kind="chunked", seed=6, batch=8, n_heads=32, n_kv_heads=8,
                                   head_dim=128, q_lens=[512] * 8, ctx_lens=(512, 7680), page_size=16,
                                   window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),

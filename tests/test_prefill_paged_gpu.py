@@ -48,6 +48,19 @@ def test_chunks(D, page_size):
     _check(case, "D=%d P=%d" % (D, page_size))
 
 
+@pytest.mark.parametrize("n_seq", [5, 40])
+def test_many_sequences_both_launch_orders(n_seq):
+    # up to 128 (sequence, query tile) pairs are ranked longest first inside the
+    # kernel; more pairs take the plain (tile, head, sequence) grid.  40 sequences
+    # of up to 4 query tiles give 160 pairs.
+    rng = np.random.default_rng(n_seq)
+    q_lens = [int(x) for x in rng.integers(0, 200, n_seq)]
+    ctx = [int(x) for x in rng.integers(0, 500, n_seq)]
+    q_lens[0] = 500   # the longest chunk sets the grid: 4 query tiles
+    case = si.make_chunked_case(n_seq, 4, 2, 128, q_lens, ctx, seed=90 + n_seq, page_size=16)
+    _check(case, "%d sequences" % n_seq)
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 2), (6, 2)])
 def test_chunks_gqa(Hq, Hkv):
     case = si.make_chunked_case(2, Hq, Hkv, 128, [64, 200], [500, 129], seed=Hq * 10 + Hkv, page_size=16)

@@ -30,7 +30,7 @@ def _sample_rows(n_outer, n_heads, k, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["tiny_decode", "paged_gqa_decode", "int8_long_decode"])
+@pytest.mark.parametrize("name", ["tiny_decode", "paged_gqa_decode", "int8_long_decode", "ring_window_decode"])
 def test_decode_workload(name):
     g = si.make_workload(name, device="cuda")
     lse = torch.empty((g.batch, g.n_heads), dtype=torch.float32, device="cuda")
