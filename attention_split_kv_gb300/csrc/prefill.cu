@@ -304,64 +304,68 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if constexpr (C::THREADS == 256) setmaxnreg_dec<C::REG_OTHER>();
         if (warp == 4) {
             // ------------------------------------------------------------ TMA producer
-            // lane 0 loads Q and the K tiles, lane 1 the V tiles; each waits only for
-            // its own stages to be released
-            if (lane == 0 || lane == 1) {
-                const bool is_k = lane == 0;
+            // Contiguous: lane 0 loads Q and the K tiles, lane 1 the V tiles.  Paged:
+            // lanes 0-15 load K and lanes 16-31 V, lane i of a group the box of the
+            // tile's i-th page (R rows; one box inside a page when pages are longer
+            // than the tile), so the boxes of a tile are issued in parallel.  A
+            // group's leader waits for the stage and posts the byte count; each
+            // group waits only for its own stages to be released.
+            const int grp_lane = PAGED ? (lane & 15) : 0;
+            if (PAGED || lane < 2) {
+                const bool is_k = PAGED ? lane < 16 : lane == 0;
+                const bool leader = grp_lane == 0;
+                const unsigned gmask = is_k ? 0x0000ffffu : 0xffff0000u;
                 const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
                 const uint32_t off = is_k ? C::OFF_K : C::OFF_V;
                 const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
                 const int NST = is_k ? C::KST : C::VST;
-                tma_prefetch_desc(tm);
-                if (is_k) {
+                if (leader) tma_prefetch_desc(tm);
+                if (is_k && leader) {
                     tma_prefetch_desc(&tm_q);
                     mbar_arrive_expect_tx(bar(B_QFULL), C::Q_BYTES);
                     for (int c = 0; c < NCH; ++c)
                         tma_load_3d(sbase + C::OFF_Q + c * (BM * 128), &tm_q, bar(B_QFULL), c * 64, h, q_base + q0);
                 }
                 int issued = 0;
-                // paged: one box of R rows per page (or one box inside a page).  The
-                // page ids of tile j+1 are loaded right after tile j's copies are
-                // issued, so their latency hides behind the wait for a free stage.
-                constexpr int MAXB = PAGED ? BN / 8 : 1;   // boxes per tile (pages >= 8 tokens)
                 const int R = PAGED ? args.box_rows : BN;
-                int pg[MAXB];
-                auto fetch_pages = [&](int j) {
-                    const int key0 = (jt0 + j) * BN;
-#pragma unroll
-                    for (int i = 0; i < MAXB; ++i) {
-                        const int kk = key0 + i * R;
-                        pg[i] = 0;
-                        if (i * R < BN && j < n_tiles && kk < L)
-                            pg[i] = __ldg(&args.page_table[(size_t)b * args.max_pages + (kk >> args.log2P)]);
-                    }
+                const bool has_box = grp_lane * R < BN;   // pages of >= 8 tokens: at most 16 boxes
+                // the page id of this lane's box in tile j+1 is loaded right after tile j's
+                // copies are issued, so its latency hides behind the wait for a free stage
+                int pg = 0;
+                auto fetch_page = [&](int j) {
+                    const int kk = (jt0 + j) * BN + grp_lane * R;
+                    pg = (has_box && j < n_tiles && kk < L)
+                             ? __ldg(&args.page_table[(size_t)b * args.max_pages + (kk >> args.log2P)]) : 0;
                 };
-                if constexpr (PAGED) fetch_pages(0);
+                if constexpr (PAGED) fetch_page(0);
                 for (int j = 0; j < n_tiles; ++j) {
                     const int st = j % NST;
-                    if (j >= NST &&
-                        !mbar_wait(bar(b_empty + st), ((j / NST) - 1) & 1, abort_flag, args.err, kErrTimeoutSlot))
-                        break;
+                    if (j >= NST) {
+                        int ok = 1;
+                        if (leader) ok = mbar_wait(bar(b_empty + st), ((j / NST) - 1) & 1, abort_flag, args.err,
+                                                   kErrTimeoutSlot);
+                        if constexpr (PAGED) ok = __shfl_sync(gmask, ok, is_k ? 0 : 16);
+                        if (!ok) break;
+                    }
                     const int key0 = (jt0 + j) * BN;
-                    mbar_arrive_expect_tx(bar(b_full + st), C::KV_BYTES);
+                    if (leader) mbar_arrive_expect_tx(bar(b_full + st), C::KV_BYTES);
                     if constexpr (PAGED) {
+                        __syncwarp(gmask);
                         // boxes past the cached keys get the page coordinate n_pages, past
                         // the pool, so the copy fills zeros instead of reading anything
-#pragma unroll
-                        for (int i = 0; i < MAXB; ++i) {
-                            if (i * R >= BN) break;
-                            const int kk = key0 + i * R;
+                        if (has_box) {
+                            const int kk = key0 + grp_lane * R;
                             int page = args.n_pages, row = 0;
                             if (kk < L) {
-                                if (pg[i] >= 0 && pg[i] < args.n_pages) page = pg[i];
+                                if (pg >= 0 && pg < args.n_pages) page = pg;
                                 else atomicExch(args.err, kErrBadPage);   // never read: reported
                                 row = kk & (args.P - 1);
                             }
                             for (int c = 0; c < NCH; ++c)
-                                tma_load_4d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK + i * R * 128, tm,
-                                            bar(b_full + st), c * 64, g, row, page);
+                                tma_load_4d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK + grp_lane * R * 128,
+                                            tm, bar(b_full + st), c * 64, g, row, page);
                         }
-                        fetch_pages(j + 1);
+                        fetch_page(j + 1);
                     } else {
                         for (int c = 0; c < NCH; ++c)
                             tma_load_3d(sbase + off + st * C::KV_BYTES + c * C::KV_CHUNK, tm, bar(b_full + st), c * 64,
@@ -369,8 +373,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     }
                     issued = j + 1;
                 }
-                if (*abort_flag) {
+                if (leader && *abort_flag) {
                     // let copies already in flight land before the CTA's shared memory goes away
+                    // (the stage's byte count covers every lane's boxes)
                     volatile int never = 0;
                     if (is_k) mbar_wait(bar(B_QFULL), 0, &never, args.err, kErrTimeoutLoad);
                     for (int j = max(0, issued - NST); j < issued; ++j)
