@@ -60,6 +60,11 @@ def _load():
             lib.oracle_prefill_paged.argtypes = [P, P, P, P, P, P, i32, i32, i64, i32, i32, i32, i32,
                                                  i32, f64, f64, i32, P, P, P, P, i32]
             lib.oracle_prefill_paged.restype = i32
+            lib.oracle_decode_tiered.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i64, i64,
+                                                 P, P, P, P, i64,
+                                                 i32, i32, i32, i32, i32, f64, f64,
+                                                 i32, P, P, P, P, i32]
+            lib.oracle_decode_tiered.restype = i32
             lib.oracle_max_threads.restype = i32
             _lib = lib
     return _lib
@@ -187,4 +192,45 @@ def prefill_paged(case, rows=None, n_threads: int = 0):
                                   n_rows, _ptr(rr), _ptr(rh), _ptr(out), _ptr(lse), int(n_threads))
     if rc != 0:
         raise ValueError("oracle_prefill_paged rejected its arguments")
+    return out, lse
+
+
+def decode_tiered(case, rows=None, n_threads: int = 0):
+    """Oracle tiered decode for a TieredCase-like object (cold cache + f16 hot ring).
+
+    rows: None for every (b, h) in row-major order, or a list of (b, h) pairs.
+    Returns (out float64 [n, D], lse float64 [n]) with lse in natural-log units.
+    """
+    lib = _load()
+    q = _f16_bits(case.q)
+    if case.int8:
+        ck = _np(case.k).astype(np.int8, copy=False)
+        cv = _np(case.v).astype(np.int8, copy=False)
+        cks, cvs = _f16_bits(case.k_scales), _f16_bits(case.v_scales)
+    else:
+        ck, cv = _f16_bits(case.k), _f16_bits(case.v)
+        cks = cvs = None
+    cold_len = _np(case.kv_len).astype(np.int32, copy=False)
+    pt = None if case.page_table is None else _np(case.page_table).astype(np.int32, copy=False)
+    hk, hv = _f16_bits(case.hot_k), _f16_bits(case.hot_v)
+    hot_len = _np(case.hot_len).astype(np.int32, copy=False)
+    hot_start = _np(case.hot_start).astype(np.int32, copy=False)
+    if rows is None:
+        n_rows, rb, rh = -1, None, None
+        n = case.batch * case.n_heads
+    else:
+        rows = np.asarray(rows, dtype=np.int32).reshape(-1, 2)
+        n_rows = n = rows.shape[0]
+        rb, rh = np.ascontiguousarray(rows[:, 0]), np.ascontiguousarray(rows[:, 1])
+    out = np.zeros((n, case.head_dim), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    n_pages = int(case.k.shape[0]) if case.page_table is not None else 0
+    rc = lib.oracle_decode_tiered(_ptr(q), _ptr(ck), _ptr(cv), int(case.int8), _ptr(cks), _ptr(cvs),
+                                  _ptr(cold_len), _ptr(pt), int(case.page_size), int(case.max_pages or 0),
+                                  int(case.cap), n_pages, _ptr(hk), _ptr(hv), _ptr(hot_len), _ptr(hot_start),
+                                  int(case.hot_ring), case.batch, case.n_heads, case.n_kv_heads, case.head_dim,
+                                  int(case.window), float(case.softcap), float(case.scale),
+                                  n_rows, _ptr(rb), _ptr(rh), _ptr(out), _ptr(lse), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_decode_tiered rejected its arguments")
     return out, lse

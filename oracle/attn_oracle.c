@@ -223,6 +223,89 @@ int oracle_decode(const uint16_t* q, const void* k, const void* v, int kv_int8,
 }
 
 /*
+ * Tiered decode (doppler attention.js, executeAttentionTiered and
+ * executeAttentionTieredQuant: a hot tier and a cold tier read in one pass,
+ * hotLayout 'ring', coldLayout 'paged' or contiguous, hotWindow, hotStart).
+ * Sequence b's keys are its cold_len[b] cold tokens followed by its
+ * hot_len[b] hot tokens:
+ *   cold token j  at position j, read from the cold cache like oracle_decode
+ *                 (contiguous [B][cold_cap][Hkv][D] or paged; f16 or int8 with
+ *                 scales); cold_len is clamped to [0, capacity];
+ *   hot token i   at position cold_len + i, read from the f16 ring
+ *                 [B][hot_ring][Hkv][D], slot (hot_start[b] + i) mod hot_ring;
+ *                 the ring holds only the newest hot_ring hot tokens.
+ * The query sits at cold_len + hot_len - 1 (the newest token); a window W > 0
+ * keeps the keys whose position is within W of it.  Positions can skip
+ * (overwritten hot tokens), so the window is applied by position here and
+ * the kept keys are then attended without further masking.
+ */
+int oracle_decode_tiered(const uint16_t* q,
+                         const void* ck, const void* cv, int cold_int8,
+                         const uint16_t* ck_scales, const uint16_t* cv_scales,
+                         const int32_t* cold_len, const int32_t* page_table,
+                         int page_size, int max_pages, long cold_cap, long n_pages,
+                         const uint16_t* hk, const uint16_t* hv,
+                         const int32_t* hot_len, const int32_t* hot_start, long hot_ring,
+                         int B, int Hq, int Hkv, int D, int window, double softcap, double scale,
+                         int n_rows, const int32_t* rows_b, const int32_t* rows_h,
+                         double* out, double* lse, int n_threads)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0 || hot_ring <= 0) return -1;
+    if (page_table && page_size <= 0) return -1;
+    int G = Hq / Hkv;
+    long n = n_rows < 0 ? (long)B * Hq : n_rows;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (long r = 0; r < n; ++r) {
+        int b = n_rows < 0 ? (int)(r / Hq) : rows_b[r];
+        int h = n_rows < 0 ? (int)(r % Hq) : rows_h[r];
+        int g = h / G;
+        long cap_b = page_table ? (long)max_pages * page_size : cold_cap;
+        long Lc = cold_len[b];
+        if (Lc < 0) Lc = 0;
+        if (Lc > cap_b) Lc = cap_b;
+        long Lh = hot_len[b];
+        if (Lh < 0) Lh = 0;
+        long h_first = Lh > hot_ring ? Lh - hot_ring : 0;    /* older hot tokens were overwritten */
+        long qpos = Lc + Lh - 1;
+        long nk = Lc + (Lh - h_first);
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1) * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1) * D);
+        for (int d = 0; d < D; ++d)
+            qd[d] = oracle_f16_to_double(q[((long)b * Hq + h) * D + d]);
+        long kept = 0;
+        for (long j = 0; j < Lc; ++j) {
+            if (window > 0 && qpos - j >= window) continue;
+            for (int d = 0; d < D; ++d) {
+                Kd[kept * D + d] = oracle_cache_value(ck, ck_scales, cold_int8, page_table, page_size,
+                                                      max_pages, cold_cap, n_pages, b, j, g, d, Hkv, D);
+                Vd[kept * D + d] = oracle_cache_value(cv, cv_scales, cold_int8, page_table, page_size,
+                                                      max_pages, cold_cap, n_pages, b, j, g, d, Hkv, D);
+            }
+            ++kept;
+        }
+        for (long i = h_first; i < Lh; ++i) {
+            if (window > 0 && qpos - (Lc + i) >= window) continue;
+            long slot = ((long)hot_start[b] + i) % hot_ring;
+            if (slot < 0) slot += hot_ring;
+            long row = (((long)b * hot_ring + slot) * Hkv + g) * (long)D;
+            for (int d = 0; d < D; ++d) {
+                Kd[kept * D + d] = oracle_f16_to_double(hk[row + d]);
+                Vd[kept * D + d] = oracle_f16_to_double(hv[row + d]);
+            }
+            ++kept;
+        }
+        /* every gathered key is kept: no further mask */
+        oracle_attend(qd, Kd, Vd, kept, D, kept - 1, 1, 0, softcap, scale, out + r * D, lse + r);
+        free(qd); free(Kd); free(Vd);
+    }
+    return 0;
+}
+
+/*
  * Prefill / vision: S queries at positions 0..S-1 over the same S keys.
  * q [S][Hq][D], k/v [S][Hkv][D] (f16 bits).  rows: n_rows (i, h) pairs, or
  * n_rows < 0 for all S*Hq in (i, h) row-major order.  out: [n][D], lse: [n].

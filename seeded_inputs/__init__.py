@@ -38,6 +38,8 @@ __all__ = [
     "make_prefill_case",
     "paged_from_contiguous",
     "ring_from_contiguous",
+    "TieredCase",
+    "make_tiered_case",
     "ChunkCase",
     "make_chunked_case",
     "WORKLOADS",
@@ -139,6 +141,34 @@ class DecodeCase:
             if t is not None:
                 kw[name] = t.to(device)
         return DecodeCase(**kw)
+
+
+@dataclass
+class TieredCase(DecodeCase):
+    """Inputs of one tiered decode call: the cold tier is the DecodeCase part
+    (``kv_len`` = cold lengths, contiguous or paged, f16 or int8) and the hot
+    tier an f16 ring:
+
+      hot_k, hot_v   f16 [B, hot_ring, Hkv, D]; hot token i of sequence b in slot
+                     (hot_start[b] + i) mod hot_ring
+      hot_len        int32 [B]: hot tokens seen (the ring keeps the newest hot_ring)
+      hot_start      int32 [B]: slot of hot token 0
+    """
+    hot_k: Optional[torch.Tensor] = None
+    hot_v: Optional[torch.Tensor] = None
+    hot_len: Optional[torch.Tensor] = None
+    hot_start: Optional[torch.Tensor] = None
+    hot_ring: int = 0
+    hot_lens: list = field(default_factory=list)
+
+    def to(self, device: str) -> "TieredCase":
+        kw = dict(self.__dict__)
+        for name in ("q", "k", "v", "kv_len", "k_scales", "v_scales", "page_table", "hot_k", "hot_v",
+                     "hot_len", "hot_start"):
+            t = kw[name]
+            if t is not None:
+                kw[name] = t.to(device)
+        return TieredCase(**kw)
 
 
 @dataclass
@@ -310,6 +340,34 @@ def ring_from_contiguous(case: DecodeCase, ring: int) -> DecodeCase:
     kw = dict(case.__dict__)
     kw.update(k=kr, v=vr, k_scales=ksr, v_scales=vsr, cap=ring, ring=ring)
     return DecodeCase(**kw)
+
+
+def make_tiered_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int, cold_lens, hot_lens,
+                     hot_ring: int, seed: int, *, hot_starts=None, int8: bool = False, page_size: int = 0,
+                     n_pages: Optional[int] = None, cap: Optional[int] = None, window: int = 0,
+                     softcap: float = 0.0, scale: Optional[float] = None, device: str = "cpu") -> TieredCase:
+    """Build a tiered decode case: the cold tier as make_decode_case builds a
+    cache (``cold_lens`` tokens, contiguous or paged, f16 or int8) and an f16 hot
+    ring of ``hot_ring`` slots holding N(0,1) values in every slot.  ``hot_lens``
+    and ``cold_lens`` are lists or (lo, hi) tuples; ``hot_starts`` defaults to
+    seeded slots in [0, hot_ring)."""
+    cold = make_decode_case(batch, n_heads, n_kv_heads, head_dim, cold_lens, seed, cap=cap, int8=int8,
+                            page_size=page_size, n_pages=n_pages, window=window, softcap=softcap,
+                            scale=scale, device=device)
+    if isinstance(hot_lens, tuple):
+        hot_lens = _lengths(batch, hot_lens[0], hot_lens[1], seed * 7 + 3)
+    hot_lens = [int(x) for x in hot_lens]
+    assert len(hot_lens) == batch
+    if hot_starts is None:
+        g = _gen(seed * 7 + 4, "cpu")
+        hot_starts = torch.randint(0, hot_ring, (batch,), generator=g).tolist()
+    shape = (batch, hot_ring, n_kv_heads, head_dim)
+    kw = dict(cold.__dict__)
+    kw.update(hot_k=f16_normal(shape, seed * 1000 + 7, device), hot_v=f16_normal(shape, seed * 1000 + 8, device),
+              hot_len=torch.tensor(hot_lens, dtype=torch.int32, device=device),
+              hot_start=torch.tensor([int(x) for x in hot_starts], dtype=torch.int32, device=device),
+              hot_ring=hot_ring, hot_lens=hot_lens)
+    return TieredCase(**kw)
 
 
 def paged_from_contiguous(case: DecodeCase, page_size: int, seed: int,

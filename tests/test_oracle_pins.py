@@ -503,3 +503,104 @@ def test_ring_matches_brute_force():
             p = scipy.special.softmax(s)
             np.testing.assert_allclose(got[b * 2 + h], p @ V, rtol=0, atol=1e-12)
             np.testing.assert_allclose(lse[b * 2 + h], scipy.special.logsumexp(s), rtol=0, atol=1e-12)
+
+
+# ---- tiered (cold cache + hot ring) decode -----------------------------------
+
+def _tiered_brute(c, b, h):
+    """Tiered decode of one (sequence, head) straight from the definition: cold
+    token j at position j, hot token i at cold_len + i in ring slot
+    (hot_start + i) mod ring, the ring holding the newest hot_ring hot tokens,
+    the window by position from the query (the newest token); scipy softmax."""
+    G = c.n_heads // c.n_kv_heads
+    g = h // G
+    cap = c.max_pages * c.page_size if c.page_table is not None else c.cap
+    Lc = min(max(int(c.kv_len[b]), 0), cap)
+    Lh = max(int(c.hot_len[b]), 0)
+    qpos = Lc + Lh - 1
+    keys, vals = [], []
+
+    def cold_row(t, which):
+        cache = c.k if which == 0 else c.v
+        scales = c.k_scales if which == 0 else c.v_scales
+        if c.page_table is not None:
+            page, r = int(c.page_table[b, t // c.page_size]), t % c.page_size
+            x = cache[page, r, g].double().numpy()
+            sc = float(scales[page, g, r]) if c.int8 else 1.0
+        else:
+            x = cache[b, t, g].double().numpy()
+            sc = float(scales[b, g, t]) if c.int8 else 1.0
+        return x * sc
+
+    for j in range(Lc):
+        if c.window > 0 and qpos - j >= c.window:
+            continue
+        keys.append(cold_row(j, 0))
+        vals.append(cold_row(j, 1))
+    for i in range(max(0, Lh - c.hot_ring), Lh):
+        if c.window > 0 and qpos - (Lc + i) >= c.window:
+            continue
+        slot = (int(c.hot_start[b]) + i) % c.hot_ring
+        keys.append(c.hot_k[b, slot, g].double().numpy())
+        vals.append(c.hot_v[b, slot, g].double().numpy())
+    if not keys:
+        return np.zeros(c.head_dim), -math.inf
+    K, V = np.stack(keys), np.stack(vals)
+    s = c.scale * (K @ c.q[b, h].double().numpy())
+    if c.softcap > 0:
+        s = c.softcap * np.tanh(s / c.softcap)
+    return scipy.special.softmax(s) @ V, scipy.special.logsumexp(s)
+
+
+@pytest.mark.parametrize("int8,page_size", [(False, 0), (True, 0), (False, 8), (True, 16)])
+@pytest.mark.parametrize("window,softcap", [(0, 0.0), (7, 0.0), (30, 20.0)])
+def test_tiered_matches_brute_force(int8, page_size, window, softcap):
+    # ragged cold and hot lengths: an empty sequence, a hot tier that has
+    # overwritten its ring (40 > 16), rings starting mid-way, windows that end
+    # inside the hot tier, inside the cold tier, or not at all
+    c = si.make_tiered_case(4, 4, 2, 16, [0, 25, 3, 50], [0, 5, 40, 16], 16, seed=61 + page_size,
+                            hot_starts=[0, 13, 7, 15], int8=int8, page_size=page_size, window=window,
+                            softcap=softcap)
+    got, lse = oracle.decode_tiered(c)
+    for b in range(4):
+        for h in range(4):
+            o, l = _tiered_brute(c, b, h)
+            np.testing.assert_allclose(got[b * 4 + h], o, rtol=0, atol=1e-12)
+            if math.isinf(l):
+                assert lse[b * 4 + h] == -math.inf
+            else:
+                np.testing.assert_allclose(lse[b * 4 + h], l, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("int8", [False, True])
+@pytest.mark.parametrize("window", [0, 12])
+def test_tiered_with_no_hot_tokens_is_decode_over_the_cold_cache(int8, window):
+    c = si.make_tiered_case(3, 4, 2, 16, [1, 40, 77], [0, 0, 0], 32, seed=63, int8=int8, page_size=16,
+                            window=window)
+    cold = si.DecodeCase(**{k: v for k, v in c.__dict__.items() if k in si.DecodeCase.__dataclass_fields__})
+    a, la = oracle.decode_tiered(c)
+    b, lb = oracle.decode(cold)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+@pytest.mark.parametrize("window", [0, 9, 30])
+def test_tiered_equals_one_contiguous_cache_of_both_tiers(window):
+    # hot tokens all still in the ring: cold tokens then hot tokens in one
+    # contiguous cache, decoded with the same window, is the same attention
+    c = si.make_tiered_case(3, 4, 2, 16, [0, 20, 33], [6, 0, 16], 16, seed=65, hot_starts=[3, 9, 15],
+                            window=window)
+    lens = [int(c.kv_len[b]) + int(c.hot_len[b]) for b in range(3)]
+    k = torch.zeros((3, 64, 2, 16), dtype=torch.float16)
+    v = torch.zeros_like(k)
+    for b in range(3):
+        Lc = int(c.kv_len[b])
+        k[b, :Lc], v[b, :Lc] = c.k[b, :Lc], c.v[b, :Lc]
+        for i in range(int(c.hot_len[b])):
+            slot = (int(c.hot_start[b]) + i) % 16
+            k[b, Lc + i], v[b, Lc + i] = c.hot_k[b, slot], c.hot_v[b, slot]
+    flat = si.DecodeCase(q=c.q, k=k, v=v, kv_len=torch.tensor(lens, dtype=torch.int32), batch=3, n_heads=4,
+                         n_kv_heads=2, head_dim=16, cap=64, window=window, scale=c.scale, lens=lens)
+    a, la = oracle.decode_tiered(c)
+    b, lb = oracle.decode(flat)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(la, lb, rtol=0, atol=1e-13)
