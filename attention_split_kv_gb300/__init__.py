@@ -19,8 +19,9 @@ __all__ = [
     "ATTN_KV_F16", "ATTN_KV_INT8", "AttnError", "AttnLibraryMissing",
     "lib_path", "load", "build", "exported_symbols",
     "attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-    "attn_decode_ring", "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate", "attn_device_status",
-    "decode", "prefill", "prefill_paged",
+    "attn_decode_ring", "attn_decode_tiered", "attn_decode_tiered_workspace_size", "attn_decode_noalloc",
+    "attn_prefill", "attn_prefill_paged", "attn_decode_validate", "attn_device_status",
+    "decode", "decode_tiered", "prefill", "prefill_paged",
 ]
 
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_EBOUNDS, ATTN_ETIMEOUT = range(6)
@@ -34,7 +35,8 @@ _lib = None
 
 # every entry point include/attn.h declares
 exported_symbols = ("attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-                    "attn_decode_ring", "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate",
+                    "attn_decode_ring", "attn_decode_tiered", "attn_decode_tiered_workspace_size",
+                    "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate",
                     "attn_device_status")
 
 
@@ -74,6 +76,11 @@ def load():
     lib.attn_decode.restype = I
     lib.attn_decode_ring.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, F, F, I, P, P, P, SZ, P]
     lib.attn_decode_ring.restype = I
+    lib.attn_decode_tiered_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.attn_decode_tiered_workspace_size.restype = SZ
+    lib.attn_decode_tiered.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, P, P, P, P, I, I, I, I, I, I, F, F, I,
+                                       P, P, P, SZ, P]
+    lib.attn_decode_tiered.restype = I
     lib.attn_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, I, I, I, I, I, F, F, I, P, P, P]
     lib.attn_decode_noalloc.restype = I
     lib.attn_prefill.argtypes = [P, P, P, I, I, I, I, I, I, F, F, P, P, P]
@@ -141,6 +148,45 @@ def attn_decode_ring(q, k_ring, v_ring, seq_len, ring_size, k_scales, v_scales, 
                                    int(n_kv_heads), int(head_dim), int(window), float(softcap), float(scale),
                                    int(split_keys), _ptr(out), _ptr(lse_out), _ptr(workspace),
                                    int(workspace_bytes), _stream(stream)))
+
+
+def attn_decode_tiered_workspace_size(batch, n_heads, n_kv_heads, head_dim, cold_max_kv, hot_ring,
+                                      split_keys=0) -> int:
+    return int(load().attn_decode_tiered_workspace_size(batch, n_heads, n_kv_heads, head_dim, cold_max_kv,
+                                                        hot_ring, split_keys))
+
+
+def attn_decode_tiered(q, cold_k, cold_v, cold_k_scales, cold_v_scales, cold_dtype, cold_len, cold_page_table,
+                       cold_page_size, cold_max_pages_per_seq, cold_n_pages, cold_max_kv, hot_k, hot_v, hot_len,
+                       hot_start, hot_ring, batch, n_heads, n_kv_heads, head_dim, window, softcap, scale,
+                       split_keys, out, lse_out, workspace, workspace_bytes, stream=None) -> None:
+    _check(load().attn_decode_tiered(_ptr(q), _ptr(cold_k), _ptr(cold_v), _ptr(cold_k_scales), _ptr(cold_v_scales),
+                                     int(cold_dtype), _ptr(cold_len), _ptr(cold_page_table), int(cold_page_size),
+                                     int(cold_max_pages_per_seq), int(cold_n_pages), int(cold_max_kv), _ptr(hot_k),
+                                     _ptr(hot_v), _ptr(hot_len), _ptr(hot_start), int(hot_ring), int(batch),
+                                     int(n_heads), int(n_kv_heads), int(head_dim), int(window), float(softcap),
+                                     float(scale), int(split_keys), _ptr(out), _ptr(lse_out), _ptr(workspace),
+                                     int(workspace_bytes), _stream(stream)))
+
+
+def decode_tiered(case, out=None, lse_out=None, workspace=None, split_keys: int = 0, stream=None):
+    """attn_decode_tiered on a TieredCase-like object (tensors already on the GPU)."""
+    import torch
+    dev = case.q.device
+    B, Hq, Hkv, D = case.batch, case.n_heads, case.n_kv_heads, case.head_dim
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=dev)
+    ws_bytes = attn_decode_tiered_workspace_size(B, Hq, Hkv, D, case.cap, case.hot_ring, split_keys)
+    if ws_bytes == 0:
+        raise AttnError(ATTN_EINVAL, "invalid sizes for the tiered decode workspace")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    attn_decode_tiered(case.q, case.k, case.v, case.k_scales, case.v_scales,
+                       ATTN_KV_INT8 if case.int8 else ATTN_KV_F16, case.kv_len, case.page_table, case.page_size,
+                       case.max_pages, case.n_pages, case.cap, case.hot_k, case.hot_v, case.hot_len,
+                       case.hot_start, case.hot_ring, B, Hq, Hkv, D, case.window, case.softcap, case.scale,
+                       split_keys, out, lse_out, workspace, workspace.numel(), stream)
+    return out
 
 
 def attn_decode_noalloc(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages,

@@ -176,13 +176,14 @@ size_t attn_decode_workspace_size(int batch, int n_heads, int n_kv_heads, int he
     return plan.bytes;
 }
 
-// attn_decode and attn_decode_ring: ring > 0 selects the ring cache
-static attn_status decode_entry(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
-                                const int32_t* page_table, int page_size, int max_pages_per_seq, int n_pages,
-                                int max_kv, const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
-                                int batch, int n_heads, int n_kv_heads, int head_dim, int window, float softcap,
-                                float scale, int split_keys, void* out, float* lse_out, void* workspace,
-                                size_t workspace_bytes, void* stream, int ring) {
+// Host checks and launch description of one decode cache (everything but the
+// workspace); ring > 0 selects the ring layout.
+static attn_status decode_prepare(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
+                                  const int32_t* page_table, int page_size, int max_pages_per_seq, int n_pages,
+                                  int max_kv, const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
+                                  int batch, int n_heads, int n_kv_heads, int head_dim, int window, float softcap,
+                                  float scale, int split_keys, void* out, float* lse_out, void* stream, int ring,
+                                  DecodeLaunch* Lp, DecodePlan* plan_p) {
     if (!q || !k_cache || !v_cache || !kv_len || !out)
         return set_error(ATTN_EINVAL, "attn_decode: q, k_cache, v_cache, kv_len and out must be non-null");
     if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0)
@@ -219,16 +220,10 @@ static attn_status decode_entry(const void* q, const void* k_cache, const void* 
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         (int8 && (!aligned(k_scales, 16) || !aligned(v_scales, 16))))
         return set_error(ATTN_EINVAL, "attn_decode: q, caches, scales and out must be 16-byte aligned");
-    DecodePlan plan;
+    DecodePlan& plan = *plan_p;
     if (!make_decode_plan(batch, n_heads, n_kv_heads, head_dim, max_kv, split_keys, &plan))
         return set_error(ATTN_EINVAL, "attn_decode: invalid sizes for the split plan");
-    if (!workspace || workspace_bytes < plan.bytes)
-        return set_error(ATTN_EINVAL, "attn_decode: workspace of %zu bytes needed, %zu given", plan.bytes,
-                         workspace ? workspace_bytes : (size_t)0);
-    if (!aligned(workspace, 256)) return set_error(ATTN_EINVAL, "attn_decode: workspace must be 256-byte aligned");
-    int* err = device_error_word();
-    if (!err) return set_error(ATTN_ECUDA, "attn_decode: no CUDA device / error word");
-    DecodeLaunch L;
+    DecodeLaunch& L = *Lp;
     L.q = q;
     L.k = k_cache;
     L.v = v_cache;
@@ -253,11 +248,106 @@ static attn_status decode_entry(const void* q, const void* k_cache, const void* 
     L.split_keys = split_keys;
     L.out = out;
     L.lse = lse_out;
+    L.stream = static_cast<cudaStream_t>(stream);
+    return ATTN_OK;
+}
+
+static attn_status check_workspace(const char* fn, void* workspace, size_t workspace_bytes, size_t need) {
+    if (!workspace || workspace_bytes < need)
+        return set_error(ATTN_EINVAL, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                         workspace ? workspace_bytes : (size_t)0);
+    if (!aligned(workspace, 256)) return set_error(ATTN_EINVAL, "%s: workspace must be 256-byte aligned", fn);
+    return ATTN_OK;
+}
+
+// attn_decode and attn_decode_ring: ring > 0 selects the ring cache
+static attn_status decode_entry(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
+                                const int32_t* page_table, int page_size, int max_pages_per_seq, int n_pages,
+                                int max_kv, const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
+                                int batch, int n_heads, int n_kv_heads, int head_dim, int window, float softcap,
+                                float scale, int split_keys, void* out, float* lse_out, void* workspace,
+                                size_t workspace_bytes, void* stream, int ring) {
+    DecodeLaunch L;
+    DecodePlan plan;
+    attn_status st = decode_prepare(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages,
+                                    max_kv, k_scales, v_scales, kv_dtype, batch, n_heads, n_kv_heads, head_dim,
+                                    window, softcap, scale, split_keys, out, lse_out, stream, ring, &L, &plan);
+    if (st != ATTN_OK) return st;
+    if ((st = check_workspace("attn_decode", workspace, workspace_bytes, plan.bytes)) != ATTN_OK) return st;
+    int* err = device_error_word();
+    if (!err) return set_error(ATTN_ECUDA, "attn_decode: no CUDA device / error word");
     L.workspace = workspace;
     L.workspace_bytes = workspace_bytes;
     L.err_word = err;
-    L.stream = static_cast<cudaStream_t>(stream);
     return launch_decode(L, plan);
+}
+
+// The two plans of a tiered decode and the workspace they share: the cold
+// tier's partials first, the hot ring's from the next 256-byte boundary.
+static bool tiered_plans(int batch, int n_heads, int n_kv_heads, int head_dim, int cold_max_kv, int hot_ring,
+                         int split_keys, DecodePlan* cold, DecodePlan* hot, size_t* hot_off, size_t* bytes) {
+    if (batch <= 0 || batch > kDecodeMaxBatch || hot_ring < 16 || hot_ring % 16 != 0) return false;
+    if (!make_decode_plan(batch, n_heads, n_kv_heads, head_dim, cold_max_kv, split_keys, cold)) return false;
+    if (!make_decode_plan(batch, n_heads, n_kv_heads, head_dim, hot_ring, split_keys, hot)) return false;
+    *hot_off = (cold->bytes + 255) / 256 * 256;
+    *bytes = *hot_off + hot->bytes;
+    return true;
+}
+
+size_t attn_decode_tiered_workspace_size(int batch, int n_heads, int n_kv_heads, int head_dim, int cold_max_kv,
+                                         int hot_ring, int split_keys) {
+    DecodePlan c, h;
+    size_t off = 0, bytes = 0;
+    if (!tiered_plans(batch, n_heads, n_kv_heads, head_dim, cold_max_kv, hot_ring, split_keys, &c, &h, &off, &bytes))
+        return 0;
+    return bytes;
+}
+
+attn_status attn_decode_tiered(const void* q, const void* cold_k, const void* cold_v, const void* cold_k_scales,
+                               const void* cold_v_scales, attn_kv_dtype cold_dtype, const int32_t* cold_len,
+                               const int32_t* cold_page_table, int cold_page_size, int cold_max_pages_per_seq,
+                               int cold_n_pages, int cold_max_kv, const void* hot_k, const void* hot_v,
+                               const int32_t* hot_len, const int32_t* hot_start, int hot_ring, int batch,
+                               int n_heads, int n_kv_heads, int head_dim, int window, float softcap, float scale,
+                               int split_keys, void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    if (!hot_k || !hot_v || !hot_len || !hot_start)
+        return set_error(ATTN_EINVAL, "attn_decode_tiered: hot_k, hot_v, hot_len and hot_start must be non-null");
+    if (hot_ring < 16 || hot_ring % 16 != 0)
+        return set_error(ATTN_EUNSUPPORTED, "attn_decode_tiered: hot_ring %d must be a positive multiple of 16",
+                         hot_ring);
+    DecodeLaunch Lc, Lh;
+    DecodePlan pc, ph;
+    attn_status st = decode_prepare(q, cold_k, cold_v, cold_len, cold_page_table, cold_page_size,
+                                    cold_max_pages_per_seq, cold_n_pages, cold_max_kv, cold_k_scales, cold_v_scales,
+                                    cold_dtype, batch, n_heads, n_kv_heads, head_dim, window, softcap, scale,
+                                    split_keys, out, lse_out, stream, 0, &Lc, &pc);
+    if (st != ATTN_OK) return st;
+    st = decode_prepare(q, hot_k, hot_v, hot_len, nullptr, 0, 0, 0, hot_ring, nullptr, nullptr, ATTN_KV_F16, batch,
+                        n_heads, n_kv_heads, head_dim, window, softcap, scale, split_keys, out, lse_out, stream,
+                        hot_ring, &Lh, &ph);
+    if (st != ATTN_OK) return st;
+    size_t hot_off = 0, bytes = 0;
+    if (!tiered_plans(batch, n_heads, n_kv_heads, head_dim, cold_max_kv, hot_ring, split_keys, &pc, &ph, &hot_off,
+                      &bytes))
+        return set_error(ATTN_EINVAL, "attn_decode_tiered: invalid sizes for the split plans");
+    if ((st = check_workspace("attn_decode_tiered", workspace, workspace_bytes, bytes)) != ATTN_OK) return st;
+    int* err = device_error_word();
+    if (!err) return set_error(ATTN_ECUDA, "attn_decode_tiered: no CUDA device / error word");
+    // the window counts positions over both tiers (tier_range): the raw value
+    Lc.tier = 1;
+    Lc.hot_len = hot_len;
+    Lc.window = window;
+    Lh.tier = 2;
+    Lh.hot_len = hot_len;
+    Lh.hot_start = hot_start;
+    Lh.window = window;
+    Lc.workspace = workspace;
+    Lc.workspace_bytes = hot_off;
+    Lh.workspace = static_cast<uint8_t*>(workspace) + hot_off;
+    Lh.workspace_bytes = bytes - hot_off;
+    Lc.err_word = Lh.err_word = err;
+    return launch_decode_tiered(Lc, pc, Lh, ph);
 }
 
 attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,

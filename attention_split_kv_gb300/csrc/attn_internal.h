@@ -79,6 +79,11 @@ struct DecodeLaunch {
     float softcap, scale;
     int split_keys;
     int ring = 0;           // > 0: contiguous ring of `ring` slots, logical token t in slot t % ring
+    // tiered decode: 1 = the cold tier (kv_len = cold lengths), 2 = the hot ring
+    // (hot token i at index hot_start + i); 0 = a plain decode
+    int tier = 0;
+    const int32_t* hot_len = nullptr;
+    const int32_t* hot_start = nullptr;
     void* out;
     float* lse;
     void* workspace;
@@ -100,6 +105,8 @@ struct DecodePlan {
 };
 bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys, DecodePlan* plan);
 attn_status launch_decode(const DecodeLaunch& L, const DecodePlan& plan);
+attn_status launch_decode_tiered(const DecodeLaunch& cold, const DecodePlan& cold_plan, const DecodeLaunch& hot,
+                                 const DecodePlan& hot_plan);
 
 constexpr int kDecodeMaxBatch = 4096;
 constexpr int kDecodeMaxFix = 256;    // most CTAs the balanced decode kernel launches (>= SMs)

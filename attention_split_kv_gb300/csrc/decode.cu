@@ -97,6 +97,11 @@ struct DecArgs {
     float* ws_fix_o;
     int B, Hq, Hkv, G, HG, U, n_hb, nh_box, split, cap_eff, window, P, R, max_pages, n_pages, paged;
     int ring;          // > 0: contiguous ring cache, logical token t in row t % ring
+    // tiered decode: kTierCold reads kv_len = cold lengths (window counted from the
+    // newest hot token), kTierHot the hot ring (hot_len, hot_start); kTierPlain alone
+    int tier;
+    const int32_t* hot_len;
+    const int32_t* hot_start;
     float qscale;      // multiplies q: scale*log2e (no cap) or scale/c (cap)
     float cap_log2;    // c*log2e, 0 when the cap is off
     int* err;
@@ -110,6 +115,36 @@ __device__ __forceinline__ void seq_range(int L, int cap_eff, int W, int& start,
     start = (W > 0) ? max(0, L - W) : 0;
     end = L;
 }
+enum : int { kTierPlain = 0, kTierCold = 1, kTierHot = 2 };
+
+// Kept keys [start, end) of sequence b in the index space of the call's cache
+// (logical tokens; for the hot ring, hot token i is index hot_start + i, read
+// from slot index % ring).  Tiered decode (attention.js executeAttentionTiered):
+// the cold tier's tokens sit at positions 0 .. cold_len-1 and the hot tier's at
+// cold_len + i, the query at cold_len + hot_len - 1; a window W keeps positions
+// within W of the query, and the ring holds only its newest `ring` hot tokens.
+// T is DecArgs or a combine tier (same field names).
+template <class T>
+__device__ __forceinline__ void tier_range(const T& A, int b, int& start, int& end) {
+    if (A.tier == kTierPlain) {
+        seq_range(__ldg(&A.kv_len[b]), A.cap_eff, A.window, start, end);
+        return;
+    }
+    const int hl = max(__ldg(&A.hot_len[b]), 0);
+    if (A.tier == kTierCold) {
+        const int L = min(max(__ldg(&A.kv_len[b]), 0), A.cap_eff);
+        start = A.window > 0 ? max(0, L - max(A.window - hl, 0)) : 0;
+        end = L;
+    } else {
+        int hs = __ldg(&A.hot_start[b]) % A.ring;
+        if (hs < 0) hs += A.ring;
+        int keep = min(hl, A.ring);
+        if (A.window > 0) keep = min(keep, A.window);
+        end = hs + hl;
+        start = end - keep;
+    }
+}
+
 // Splits of a sequence: aligned to 16 tokens so that tiles start on multiples
 // of the tile (and so on page boundaries for pages of >= 16 tokens).
 __device__ __forceinline__ int seq_splits(int start, int end, int split) {
@@ -131,7 +166,7 @@ __device__ __forceinline__ Item decode_item(int it, const int* pref, const DecAr
     }
     Item r;
     r.b = lo;
-    seq_range(__ldg(&A.kv_len[lo]), A.cap_eff, A.window, r.start, r.end);
+    tier_range(A, lo, r.start, r.end);
     const int ns = seq_splits(r.start, r.end, A.split);
     const int rem = it - pref[lo];
     r.hb = rem / ns;
@@ -153,7 +188,7 @@ __device__ void build_prefix_of(const DecArgs& A, int* pref, int* scratch, F cou
         int v = 0;
         if (b < A.B) {
             int start, end;
-            seq_range(__ldg(&A.kv_len[b]), A.cap_eff, A.window, start, end);
+            tier_range(A, b, start, end);
             v = count(start, end);
         }
         int x = v;
@@ -617,14 +652,31 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
 #include "decode_tc.cuh"
 
-// One warp per (sequence, query head): log-sum-exp merge of the splits.
-template <int D>
+// One tier of the combine: where a split kernel left its partials, and the
+// range arguments that say which items it wrote.
+struct CombTier {
+    const int32_t* kv_len;
+    const int32_t* hot_len;
+    const int32_t* hot_start;
+    int tier, cap_eff, window, ring, split, n_fix;
+    const int32_t* ws_prefix;
+    const float* ws_lse;
+    const float* ws_o;
+    const int32_t* fix_meta;
+    const float* fix_lse;
+    const float* fix_o;
+};
+template <int NT>
+struct CombTiers {
+    CombTier t[NT];
+};
+
+// One warp per (sequence, query head): log-sum-exp merge of the splits of
+// every tier (one tier for a plain decode; cold and hot for a tiered decode).
+template <int D, int NT>
 __global__ void __launch_bounds__(128)
-decode_combine_kernel(const int32_t* __restrict__ kv_len, const int32_t* __restrict__ ws_prefix,
-                      const float* __restrict__ ws_lse, const float* __restrict__ ws_o, __half* __restrict__ out,
-                      float* __restrict__ lse_out, int B, int Hq, int G, int GH, int HG, int split, int cap_eff,
-                      int window, const int32_t* __restrict__ fix_meta, const float* __restrict__ fix_lse,
-                      const float* __restrict__ fix_o, int n_fix, int n_hb) {
+decode_combine_kernel(const CombTiers<NT> T, __half* __restrict__ out, float* __restrict__ lse_out, int B, int Hq,
+                      int G, int GH, int HG, int n_hb) {
     constexpr int DPL = D / 32;   // dims per lane
     // launched as a programmatic dependent of the split kernel: wait until that
     // grid has finished and its partials are visible
@@ -635,30 +687,37 @@ decode_combine_kernel(const int32_t* __restrict__ kv_len, const int32_t* __restr
     const int b = gw / Hq, h = gw - b * Hq;
     const int g = h / G, r = h - g * G, hg = r / GH, hs = r - hg * GH;
     const int u = g * HG + hg, hb = u / NW, w = u - hb * NW;
-    int start, end;
-    seq_range(kv_len[b], cap_eff, window, start, end);
-    const int ns = seq_splits(start, end, split);
-    const int item0 = ws_prefix[b] + hb * ns;
-    auto lrow = [&](int sp) { return ((size_t)(item0 + sp) * NW + w) * GH + hs; };
     const int fid = b * n_hb + hb;     // fix-up slots written for this (sequence, head block)
-    // the lse of the first KR*32 splits and every fix-up tag, as independent loads
-    // kept in registers (both passes below use them)
+    // per tier: the lse of the first KR*32 splits and every fix-up tag, as
+    // independent loads kept in registers (both passes below use them)
     constexpr int KR = 4, KF = kDecodeMaxFix / 32;
-    float lsr[KR];
-#pragma unroll
-    for (int k = 0; k < KR; ++k) lsr[k] = (k * 32 + lane < ns) ? ws_lse[lrow(k * 32 + lane)] : -INFINITY;
-    bool mine[KF];
-#pragma unroll
-    for (int q = 0; q < KF; ++q) mine[q] = (q * 32 + lane < n_fix) && fix_meta[q * 32 + lane] == fid;
-    float fls[KF];
-#pragma unroll
-    for (int q = 0; q < KF; ++q) fls[q] = mine[q] ? fix_lse[((size_t)(q * 32 + lane) * NW + w) * GH + hs] : -INFINITY;
+    int ns[NT] = {}, item0[NT] = {};
+    float lsr[NT][KR];
+    bool mine[NT][KF];
+    float fls[NT][KF];
+    auto lrow = [&](int ti, int sp) { return ((size_t)(item0[ti] + sp) * NW + w) * GH + hs; };
     float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < KR; ++k) M = fmaxf(M, lsr[k]);
-    for (int sp = KR * 32 + lane; sp < ns; sp += 32) M = fmaxf(M, ws_lse[lrow(sp)]);
+    for (int ti = 0; ti < NT; ++ti) {
+        const CombTier& t = T.t[ti];
+        int start, end;
+        tier_range(t, b, start, end);
+        ns[ti] = seq_splits(start, end, t.split);
+        item0[ti] = t.ws_prefix[b] + hb * ns[ti];
 #pragma unroll
-    for (int q = 0; q < KF; ++q) M = fmaxf(M, fls[q]);
+        for (int k = 0; k < KR; ++k)
+            lsr[ti][k] = (k * 32 + lane < ns[ti]) ? t.ws_lse[lrow(ti, k * 32 + lane)] : -INFINITY;
+#pragma unroll
+        for (int q = 0; q < KF; ++q) mine[ti][q] = (q * 32 + lane < t.n_fix) && t.fix_meta[q * 32 + lane] == fid;
+#pragma unroll
+        for (int q = 0; q < KF; ++q)
+            fls[ti][q] = mine[ti][q] ? t.fix_lse[((size_t)(q * 32 + lane) * NW + w) * GH + hs] : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < KR; ++k) M = fmaxf(M, lsr[ti][k]);
+        for (int sp = KR * 32 + lane; sp < ns[ti]; sp += 32) M = fmaxf(M, t.ws_lse[lrow(ti, sp)]);
+#pragma unroll
+        for (int q = 0; q < KF; ++q) M = fmaxf(M, fls[ti][q]);
+    }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float acc[DPL];
@@ -690,53 +749,57 @@ decode_combine_kernel(const int32_t* __restrict__ kv_len, const int32_t* __restr
     };
     auto weight = [&](float ls) { return (ls == -INFINITY) ? 0.f : ex2_approx(ls - M); };
     if (M > -INFINITY) {
-        // 32 splits at a time: lane l holds the weight of split base+l, then the
-        // warp reads the partial rows 8 at a time, all loads in flight together
-        for (int base = 0; base < ns; base += 32) {
-            const int k32 = base / 32;
-            float ls = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < KR; ++k)
-                if (k == k32) ls = lsr[k];
-            if (k32 >= KR && base + lane < ns) ls = ws_lse[lrow(base + lane)];
-            const float wl = weight(ls);
-            wl_sum += wl;
-            // the splits with weight (the rest were merged into another row or saw
-            // no key), read 8 at a time with all loads in flight together
-            unsigned mk = __ballot_sync(0xffffffffu, wl != 0.f);
-            while (mk) {
-                float v[8][DPL];
-                float wt[8];
-                const int k_first = __ffs(mk) - 1;
+        for (int ti = 0; ti < NT; ++ti) {
+            const CombTier& t = T.t[ti];
+            // 32 splits at a time: lane l holds the weight of split base+l, then the
+            // warp reads the partial rows 8 at a time, all loads in flight together
+            for (int base = 0; base < ns[ti]; base += 32) {
+                const int k32 = base / 32;
+                float ls = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    int k = k_first;
-                    wt[q] = 0.f;
-                    if (mk) {
-                        k = __ffs(mk) - 1;
-                        mk &= mk - 1;
-                        wt[q] = __shfl_sync(0xffffffffu, wl, k);
+                for (int k = 0; k < KR; ++k)
+                    if (k == k32) ls = lsr[ti][k];
+                if (k32 >= KR && base + lane < ns[ti]) ls = t.ws_lse[lrow(ti, base + lane)];
+                const float wl = weight(ls);
+                wl_sum += wl;
+                // the splits with weight (the rest were merged into another row or saw
+                // no key), read 8 at a time with all loads in flight together
+                unsigned mk = __ballot_sync(0xffffffffu, wl != 0.f);
+                while (mk) {
+                    float v[8][DPL];
+                    float wt[8];
+                    const int k_first = __ffs(mk) - 1;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        int k = k_first;
+                        wt[q] = 0.f;
+                        if (mk) {
+                            k = __ffs(mk) - 1;
+                            mk &= mk - 1;
+                            wt[q] = __shfl_sync(0xffffffffu, wl, k);
+                        }
+                        load_row(t.ws_o, lrow(ti, base + k), v[q]);
                     }
-                    load_row(ws_o, lrow(base + k), v[q]);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) accumulate(wt[q], v[q]);
                 }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) accumulate(wt[q], v[q]);
             }
-        }
-        // the fix-up slots of this (sequence, head block)
+            // the fix-up slots of this (sequence, head block)
 #pragma unroll
-        for (int q = 0; q < KF; ++q) {
-            const float wl = weight(fls[q]);
-            wl_sum += wl;
-            unsigned m = __ballot_sync(0xffffffffu, mine[q]);
-            while (m) {
-                const int k = __ffs(m) - 1;
-                m &= m - 1;
-                const float wt = __shfl_sync(0xffffffffu, wl, k);
-                if (wt != 0.f) {
-                    float v[DPL];
-                    load_row(fix_o, ((size_t)(q * 32 + k) * NW + w) * GH + hs, v);
-                    accumulate(wt, v);
+            for (int q = 0; q < KF; ++q) {
+                const float wl = weight(fls[ti][q]);
+                wl_sum += wl;
+                unsigned m = __ballot_sync(0xffffffffu, mine[ti][q]);
+                while (m) {
+                    const int k = __ffs(m) - 1;
+                    m &= m - 1;
+                    const float wt = __shfl_sync(0xffffffffu, wl, k);
+                    if (wt != 0.f) {
+                        float v[DPL];
+                        load_row(t.fix_o, ((size_t)(q * 32 + k) * NW + w) * GH + hs, v);
+                        accumulate(wt, v);
+                    }
                 }
             }
         }
@@ -780,6 +843,9 @@ DecArgs make_dec_args(const DecodeLaunch& L, const DecodePlan& plan, int R) {
     // a ring holds the newest `ring` tokens of sequences of any length: no clamp
     a.cap_eff = L.ring > 0 ? (1 << 30) : (cap_layout < L.max_kv ? cap_layout : L.max_kv);
     a.ring = L.ring;
+    a.tier = L.tier;
+    a.hot_len = L.hot_len;
+    a.hot_start = L.hot_start;
     a.window = L.window;
     a.P = paged ? L.page_size : 0;
     a.R = R;
@@ -793,15 +859,42 @@ DecArgs make_dec_args(const DecodeLaunch& L, const DecodePlan& plan, int R) {
     return a;
 }
 
-// n_fix: fix-up slots the split kernel wrote (its grid for the balanced
-// tensor-core kernel, 0 for the item-per-CTA kernel)
+// What a split kernel launch leaves for the combine: its arguments and the
+// fix-up slots it wrote (its grid for the balanced tensor-core kernel, 0 for
+// the item-per-CTA kernel).
+struct SplitOut {
+    DecArgs a;
+    int n_fix;
+};
+
+CombTier comb_tier(const SplitOut& so) {
+    const DecArgs& a = so.a;
+    CombTier t;
+    t.kv_len = a.kv_len;
+    t.hot_len = a.hot_len;
+    t.hot_start = a.hot_start;
+    t.tier = a.tier;
+    t.cap_eff = a.cap_eff;
+    t.window = a.window;
+    t.ring = a.ring;
+    t.split = a.split;
+    t.n_fix = so.n_fix;
+    t.ws_prefix = a.ws_prefix;
+    t.ws_lse = a.ws_lse;
+    t.ws_o = a.ws_o;
+    t.fix_meta = a.ws_fix_meta;
+    t.fix_lse = a.ws_fix_lse;
+    t.fix_o = a.ws_fix_o;
+    return t;
+}
+
 // The combine is a programmatic dependent launch: its CTAs may be scheduled
 // while the split kernel's last CTAs finish (hiding the launch latency) and
-// wait in griddepcontrol.wait for that grid to complete.
-// n_fix: fix-up slots the split kernel wrote (its grid for the balanced
-// tensor-core kernel, 0 for the item-per-CTA kernel)
-template <int D>
-attn_status launch_combine(const DecodeLaunch& L, const DecodePlan& plan, const DecArgs& a, int n_fix) {
+// wait in griddepcontrol.wait for that grid to complete.  (A tiered decode's
+// cold split kernel finished before its hot split kernel started: plain stream
+// order.)
+template <int D, int NT>
+attn_status launch_combine(const DecodeLaunch& L, const DecodePlan& plan, const CombTiers<NT>& T) {
     const int nwarps = L.B * L.Hq;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((nwarps + 3) / 4);
@@ -813,14 +906,20 @@ attn_status launch_combine(const DecodeLaunch& L, const DecodePlan& plan, const 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, L.kv_len, (const int32_t*)a.ws_prefix,
-                                       (const float*)a.ws_lse, (const float*)a.ws_o, static_cast<__half*>(L.out), L.lse,
-                                       L.B, L.Hq, a.G, plan.GH, plan.HG, plan.split, a.cap_eff, L.window,
-                                       (const int32_t*)a.ws_fix_meta, (const float*)a.ws_fix_lse,
-                                       (const float*)a.ws_fix_o, n_fix, plan.n_hb);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, NT>, T, static_cast<__half*>(L.out), L.lse,
+                                       L.B, L.Hq, L.Hq / L.Hkv, plan.GH, plan.HG, plan.n_hb);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode combine launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
+}
+
+template <int NT>
+attn_status launch_combine_d(const DecodeLaunch& L, const DecodePlan& plan, const CombTiers<NT>& T) {
+    switch (L.D) {
+        case 64: return launch_combine<64, NT>(L, plan, T);
+        case 128: return launch_combine<128, NT>(L, plan, T);
+        default: return launch_combine<256, NT>(L, plan, T);
+    }
 }
 
 int decode_grid(const DecodePlan& plan) {
@@ -831,7 +930,7 @@ int decode_grid(const DecodePlan& plan) {
 
 // Tensor-core split kernel: f16 caches, head_dim 64/128, boxes of 16 rows x NH heads.
 template <int D, int NH>
-attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan) {
+attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, SplitOut* so) {
     using C = tcdec::Cfg<D>;
     const bool paged = L.page_table != nullptr;
     CUtensorMap tq, tk, tv;
@@ -876,11 +975,13 @@ attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan) {
     tcdec::decode_tc_kernel<D, NH><<<grid, tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a, q_rows);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode tc launch failed: %s", cudaGetErrorString(e));
-    return launch_combine<D>(L, plan, a, grid);
+    so->a = a;
+    so->n_fix = grid;
+    return ATTN_OK;
 }
 
 template <int D, bool I8, int GH>
-attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
+attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan, SplitOut* so) {
     using C = DecCfg<D, I8, GH>;
     const int esz = I8 ? 1 : 2;
     const CUtensorMapDataType kvt = I8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -893,10 +994,10 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
         while (nh < plan.nh_box) nh <<= 1;
         if ((!paged || L.page_size % 16 == 0) && nh <= L.Hkv && L.B <= tcdec::kMaxBatch) {
             switch (nh) {
-                case 1: return launch_decode_tc<D, 1>(L, plan);
-                case 2: return launch_decode_tc<D, 2>(L, plan);
-                case 4: return launch_decode_tc<D, 4>(L, plan);
-                default: return launch_decode_tc<D, 8>(L, plan);
+                case 1: return launch_decode_tc<D, 1>(L, plan, so);
+                case 2: return launch_decode_tc<D, 2>(L, plan, so);
+                case 4: return launch_decode_tc<D, 4>(L, plan, so);
+                default: return launch_decode_tc<D, 8>(L, plan, so);
             }
         }
     }
@@ -947,15 +1048,27 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan) {
     decode_split_kernel<D, I8, GH><<<decode_grid(plan), kDecThreads, C::SMEM_ALLOC, L.stream>>>(tk, tv, tks, tvs, a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode split launch failed: %s", cudaGetErrorString(e));
-    return launch_combine<D>(L, plan, a, 0);
+    so->a = a;
+    so->n_fix = 0;
+    return ATTN_OK;
 }
 
 template <int D, bool I8>
-attn_status launch_decode_gh(const DecodeLaunch& L, const DecodePlan& plan) {
+attn_status launch_decode_gh(const DecodeLaunch& L, const DecodePlan& plan, SplitOut* so) {
     switch (plan.GH) {
-        case 4: return launch_decode_t<D, I8, 4>(L, plan);
-        case 2: return launch_decode_t<D, I8, 2>(L, plan);
-        default: return launch_decode_t<D, I8, 1>(L, plan);
+        case 4: return launch_decode_t<D, I8, 4>(L, plan, so);
+        case 2: return launch_decode_t<D, I8, 2>(L, plan, so);
+        default: return launch_decode_t<D, I8, 1>(L, plan, so);
+    }
+}
+
+// The split kernel for one cache (either kernel; see launch_decode_t).
+attn_status launch_split(const DecodeLaunch& L, const DecodePlan& plan, SplitOut* so) {
+    switch (L.D) {
+        case 64: return L.int8 ? launch_decode_gh<64, true>(L, plan, so) : launch_decode_gh<64, false>(L, plan, so);
+        case 128: return L.int8 ? launch_decode_gh<128, true>(L, plan, so) : launch_decode_gh<128, false>(L, plan, so);
+        case 256: return L.int8 ? launch_decode_gh<256, true>(L, plan, so) : launch_decode_gh<256, false>(L, plan, so);
+        default: return set_error(ATTN_EUNSUPPORTED, "head_dim %d not supported (64, 128, 256)", L.D);
     }
 }
 
@@ -1012,12 +1125,27 @@ bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys,
 }
 
 attn_status launch_decode(const DecodeLaunch& L, const DecodePlan& plan) {
-    switch (L.D) {
-        case 64: return L.int8 ? launch_decode_gh<64, true>(L, plan) : launch_decode_gh<64, false>(L, plan);
-        case 128: return L.int8 ? launch_decode_gh<128, true>(L, plan) : launch_decode_gh<128, false>(L, plan);
-        case 256: return L.int8 ? launch_decode_gh<256, true>(L, plan) : launch_decode_gh<256, false>(L, plan);
-        default: return set_error(ATTN_EUNSUPPORTED, "head_dim %d not supported (64, 128, 256)", L.D);
-    }
+    SplitOut so;
+    attn_status st = launch_split(L, plan, &so);
+    if (st != ATTN_OK) return st;
+    CombTiers<1> T;
+    T.t[0] = comb_tier(so);
+    return launch_combine_d<1>(L, plan, T);
+}
+
+// Tiered decode: the cold tier's split kernel, then the hot ring's, then one
+// combine over the partials of both (the two launches share out, lse and the
+// stream; each has its own plan and part of the workspace).
+attn_status launch_decode_tiered(const DecodeLaunch& cold, const DecodePlan& cold_plan, const DecodeLaunch& hot,
+                                 const DecodePlan& hot_plan) {
+    SplitOut sc, sh;
+    attn_status st = launch_split(cold, cold_plan, &sc);
+    if (st != ATTN_OK) return st;
+    if ((st = launch_split(hot, hot_plan, &sh)) != ATTN_OK) return st;
+    CombTiers<2> T;
+    T.t[0] = comb_tier(sc);
+    T.t[1] = comb_tier(sh);
+    return launch_combine_d<2>(cold, cold_plan, T);
 }
 
 }  // namespace attn

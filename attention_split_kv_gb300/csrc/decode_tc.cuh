@@ -120,7 +120,7 @@ __device__ __forceinline__ void tcur_locate(TileCur& c, const int* tpref, const 
         if (tpref[mid] <= c.x) lo = mid; else hi = mid;
     }
     c.b = lo;
-    seq_range(__ldg(&A.kv_len[lo]), A.cap_eff, A.window, c.start, c.end);
+    tier_range(A, lo, c.start, c.end);
     c.a = (c.start / 16) * 16;
     c.Tb = (tpref[lo + 1] - tpref[lo]) / A.n_hb;
     const int rel = c.x - tpref[lo];

@@ -154,6 +154,56 @@ attn_status attn_decode_ring(const void* q, const void* k_ring, const void* v_ri
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_tiered -- decode over two tiers of one sequence's cache in one
+ * call: a cold tier (the older tokens: contiguous or paged, f16 or int8 with
+ * scales) and a hot tier (the newest tokens: an f16 ring).  (doppler
+ * attention.js executeAttentionTiered / executeAttentionTieredQuant: coldLen,
+ * hotLen, hotWindow, hotStart, coldPageTable, coldPageSize, coldLayout paged
+ * or contiguous, hotLayout ring.)
+ *
+ *  cold_*      the cold tier exactly as attn_decode takes a cache:
+ *                cold_k/cold_v, cold_k_scales/cold_v_scales (int8 only),
+ *                cold_dtype, cold_len (kv_len: cold tokens of each sequence,
+ *                clamped to the capacity), cold_page_table (NULL for
+ *                contiguous [B, cold_max_kv, Hkv, D]), cold_page_size,
+ *                cold_max_pages_per_seq, cold_n_pages, cold_max_kv (contiguous
+ *                capacity, or paged bound).  Same rules and errors.
+ *  hot_k,      device f16 [B, hot_ring, Hkv, D]: hot token i of sequence b in
+ *  hot_v         slot (hot_start[b] + i) mod hot_ring.
+ *  hot_len     device int32 [B]: hot tokens of each sequence (<= 0: none).
+ *                The ring holds the newest hot_ring of them; older ones are
+ *                gone.
+ *  hot_start   device int32 [B]: slot of hot token 0 (any integer; taken
+ *                modulo hot_ring).
+ *  hot_ring    slots per sequence, a positive multiple of 16
+ *                (ATTN_EUNSUPPORTED otherwise).
+ *  Positions: cold token j at j, hot token i at cold_len + i; the query is the
+ *  newest token, at cold_len + hot_len - 1.  window W > 0 keeps the keys whose
+ *  position is within W of the query (it may end inside either tier); 0 = off.
+ *  The other arguments are those of attn_decode; out and lse_out receive one
+ *  softmax over the kept keys of both tiers.  A sequence with no kept key gets
+ *  a zero row and lse = -inf.
+ *  workspace   >= attn_decode_tiered_workspace_size(B, Hq, Hkv, D,
+ *                cold_max_kv, hot_ring, split_keys) bytes, 256-byte aligned.
+ *  Three kernels run on the stream: the cold tier's split kernel, the hot
+ *  tier's, and one log-sum-exp combine over both.
+ */
+size_t attn_decode_tiered_workspace_size(int batch, int n_heads, int n_kv_heads, int head_dim,
+                                         int cold_max_kv, int hot_ring, int split_keys);
+attn_status attn_decode_tiered(const void* q,
+                               const void* cold_k, const void* cold_v,
+                               const void* cold_k_scales, const void* cold_v_scales,
+                               attn_kv_dtype cold_dtype, const int32_t* cold_len,
+                               const int32_t* cold_page_table, int cold_page_size,
+                               int cold_max_pages_per_seq, int cold_n_pages, int cold_max_kv,
+                               const void* hot_k, const void* hot_v,
+                               const int32_t* hot_len, const int32_t* hot_start, int hot_ring,
+                               int batch, int n_heads, int n_kv_heads, int head_dim,
+                               int window, float softcap, float scale, int split_keys,
+                               void* out, float* lse_out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
  * memory, so cannot supply a workspace: for example a plugin running inside
  * an engine that owns all device memory and offers it no allocator, or a

@@ -126,6 +126,47 @@ def test_decode_ring_rejects_bad_arguments_on_host(lib, kw, status):
     assert attn.attn_last_error()
 
 
+def _decode_tiered(**kw):
+    args = dict(q=FAKE, cold_k=FAKE, cold_v=FAKE, cold_k_scales=None, cold_v_scales=None,
+                cold_dtype=attn.ATTN_KV_F16, cold_len=FAKE, cold_page_table=None, cold_page_size=0,
+                cold_max_pages_per_seq=0, cold_n_pages=0, cold_max_kv=128, hot_k=FAKE, hot_v=FAKE, hot_len=FAKE,
+                hot_start=FAKE, hot_ring=64, batch=1, n_heads=4, n_kv_heads=2, head_dim=64, window=0, softcap=0.0,
+                scale=0.125, split_keys=0, out=FAKE, lse_out=None, workspace=FAKE, workspace_bytes=1 << 30,
+                stream=0)
+    args.update(kw)
+    return attn.load().attn_decode_tiered(*[args[k] for k in (
+        "q", "cold_k", "cold_v", "cold_k_scales", "cold_v_scales", "cold_dtype", "cold_len", "cold_page_table",
+        "cold_page_size", "cold_max_pages_per_seq", "cold_n_pages", "cold_max_kv", "hot_k", "hot_v", "hot_len",
+        "hot_start", "hot_ring", "batch", "n_heads", "n_kv_heads", "head_dim", "window", "softcap", "scale",
+        "split_keys", "out", "lse_out", "workspace", "workspace_bytes", "stream")])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(hot_ring=0), attn.ATTN_EUNSUPPORTED),
+    (dict(hot_ring=24), attn.ATTN_EUNSUPPORTED),
+    (dict(hot_start=None), attn.ATTN_EINVAL),
+    (dict(hot_k=None), attn.ATTN_EINVAL),
+    (dict(cold_len=None), attn.ATTN_EINVAL),
+    (dict(cold_dtype=attn.ATTN_KV_INT8), attn.ATTN_EINVAL),            # cold scales missing
+    (dict(cold_page_table=FAKE, cold_page_size=12, cold_max_pages_per_seq=4, cold_n_pages=4),
+     attn.ATTN_EUNSUPPORTED),
+    (dict(head_dim=80), attn.ATTN_EUNSUPPORTED),
+    (dict(workspace_bytes=64), attn.ATTN_EINVAL),
+    (dict(hot_v=FAKE + 4), attn.ATTN_EINVAL),                            # misaligned
+])
+def test_decode_tiered_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _decode_tiered(**kw) == status
+    assert attn.attn_last_error()
+
+
+def test_tiered_workspace_is_both_plans(lib):
+    a = attn.attn_decode_workspace_size(4, 32, 8, 128, 8192)
+    h = attn.attn_decode_workspace_size(4, 32, 8, 128, 1024)
+    t = attn.attn_decode_tiered_workspace_size(4, 32, 8, 128, 8192, 1024)
+    assert t >= a + h and t < a + h + 256
+    assert attn.attn_decode_tiered_workspace_size(4, 32, 8, 128, 8192, 1000) == 0    # ring % 16
+
+
 def _prefill(**kw):
     args = dict(q=FAKE, k=FAKE, v=FAKE, seq_len=128, n_heads=4, n_kv_heads=2, head_dim=64, causal=1,
                 window=0, softcap=0.0, scale=0.125, out=FAKE, lse_out=None, stream=0)
