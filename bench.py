@@ -11,6 +11,7 @@ masks, online softmax, PV, split combine, tensor-core prefill tiles):
   int8_long_decode     B=16, 32q/8kv heads, D=128, kv_len 32768, int8 K/V + f16 scales
   chunked_prefill_paged  B=8, 512-token chunks on 512..7680 cached tokens, 16-token pages
   ring_window_decode   B=32, 32q/8kv heads, D=128, 4096-slot ring, logical kv_len 4K..64K
+  tiered_int8_decode   B=32, 32q/8kv heads, D=128, int8 paged cold tier 2K..16K + f16 1024-slot hot ring
 
 The headline metric is the vision workload's TFLOP/s (algorithmic FLOPs
 4*S^2*D*H over the call's CUDA-event time); decode workloads report KV GB/s.
@@ -56,7 +57,7 @@ NCU_TRAFFIC = {
 }
 METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
 WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode",
-                  "chunked_prefill_paged", "ring_window_decode"]
+                  "chunked_prefill_paged", "ring_window_decode", "tiered_int8_decode"]
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -123,6 +124,30 @@ def decode_bytes(case):
     return kv + qo + case.batch * 4 + pages * 4
 
 
+def tiered_bytes(case):
+    """KV bytes a tiered decode call must read once: the kept cold tokens (codes
+    and scales for int8), the kept hot tokens (f16), plus q, out, the length and
+    start arrays and the cold page table."""
+    esz = 1 if case.int8 else 2
+    cold_tok = case.n_kv_heads * case.head_dim * esz * 2 + (case.n_kv_heads * 2 * 2 if case.int8 else 0)
+    hot_tok = case.n_kv_heads * case.head_dim * 2 * 2
+    cap = case.max_pages * case.page_size if case.paged else case.cap
+    kv = pages = 0
+    for Lc, Lh in zip(case.lens, case.hot_lens):
+        Lc = min(max(Lc, 0), cap)
+        Lh = max(Lh, 0)
+        hk = min(Lh, case.hot_ring)
+        ck = Lc
+        if case.window > 0:
+            hk = min(hk, case.window)
+            ck = max(0, min(Lc, case.window - Lh))
+        kv += ck * cold_tok + hk * hot_tok
+        if case.paged:
+            pages += (Lc + case.page_size - 1) // case.page_size
+    qo = 2 * case.batch * case.n_heads * case.head_dim * 2
+    return kv + qo + 3 * case.batch * 4 + pages * 4
+
+
 def workload_config(case):
     if hasattr(case, "q_lens"):
         return {"global_batch": case.batch, "chunk_tokens": case.total_q, "n_heads": case.n_heads,
@@ -133,6 +158,11 @@ def workload_config(case):
         return {"seq_len": case.seq_len, "n_heads": case.n_heads, "n_kv_heads": case.n_kv_heads,
                 "head_dim": case.head_dim, "causal": bool(case.causal), "window": case.window,
                 "softcap": case.softcap}
+    if hasattr(case, "hot_ring"):
+        return {"global_batch": case.batch, "n_heads": case.n_heads, "n_kv_heads": case.n_kv_heads,
+                "head_dim": case.head_dim, "cold_len_min": min(case.lens), "cold_len_max": max(case.lens),
+                "cold_kv_dtype": "int8" if case.int8 else "f16", "cold_page_size": case.page_size,
+                "hot_ring": case.hot_ring, "hot_len_min": min(case.hot_lens), "hot_len_max": max(case.hot_lens)}
     return {"global_batch": case.batch, "n_heads": case.n_heads, "n_kv_heads": case.n_kv_heads,
             "head_dim": case.head_dim, "kv_len_min": min(case.lens), "kv_len_max": max(case.lens),
             "kv_dtype": "int8" if case.int8 else "f16", "page_size": case.page_size,
@@ -341,6 +371,13 @@ def main(argv=None):
             out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float16, device=dev)
             runs[n] = (lambda c=c, ws=ws, out=out: attn.decode(c, out=out, workspace=ws))
             work[n] = ("GB/s", decode_bytes(c), "hbm", 2)
+        elif si.WORKLOADS[n]["kind"] == "tiered":
+            ws = torch.empty(attn.attn_decode_tiered_workspace_size(c.batch, c.n_heads, c.n_kv_heads, c.head_dim,
+                                                                    c.cap, c.hot_ring), dtype=torch.uint8,
+                             device=dev)
+            out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float16, device=dev)
+            runs[n] = (lambda c=c, ws=ws, out=out: attn.decode_tiered(c, out=out, workspace=ws))
+            work[n] = ("GB/s", tiered_bytes(c), "hbm", 3)
         elif si.WORKLOADS[n]["kind"] == "chunked":
             out = torch.empty_like(c.q)
             runs[n] = (lambda c=c, out=out: attn.prefill_paged(c, out=out))

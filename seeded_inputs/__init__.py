@@ -488,6 +488,12 @@ WORKLOADS = {
     "ring_window_decode": dict(kind="decode", seed=7, batch=32, n_heads=32, n_kv_heads=8, head_dim=128,
                                lens=(4096, 65536), int8=False, page_size=0, ring=4096, window=0,
                                softcap=0.0, scale=1.0 / math.sqrt(128.0)),
+    # tiered decode, the int8 tier of the pages: 32 sequences, an int8 cold tier of
+    # 2K..16K tokens on 16-token pages plus an f16 hot ring of 1024 slots holding
+    # the newest 256..1024 tokens
+    "tiered_int8_decode": dict(kind="tiered", seed=8, batch=32, n_heads=32, n_kv_heads=8, head_dim=128,
+                               cold_lens=(2048, 16384), hot_lens=(256, 1024), hot_ring=1024, int8=True,
+                               page_size=16, window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
     "chunked_prefill_paged": dict(kind="chunked", seed=6, batch=8, n_heads=32, n_kv_heads=8,
                                   head_dim=128, q_lens=[512] * 8, ctx_lens=(512, 7680), page_size=16,
                                   window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
@@ -514,6 +520,10 @@ def make_workload(name: str, device: str = "cpu"):
         b, hq, hkv, d, lens = (w.pop("batch"), w.pop("n_heads"), w.pop("n_kv_heads"),
                                w.pop("head_dim"), w.pop("lens"))
         return make_decode_case(b, hq, hkv, d, lens, seed, device=device, **w)
+    if kind == "tiered":
+        b, hq, hkv, d = w.pop("batch"), w.pop("n_heads"), w.pop("n_kv_heads"), w.pop("head_dim")
+        return make_tiered_case(b, hq, hkv, d, w.pop("cold_lens"), w.pop("hot_lens"), w.pop("hot_ring"), seed,
+                                device=device, **w)
     if kind == "chunked":
         b, hq, hkv, d = w.pop("batch"), w.pop("n_heads"), w.pop("n_kv_heads"), w.pop("head_dim")
         return make_chunked_case(b, hq, hkv, d, w.pop("q_lens"), w.pop("ctx_lens"), seed, device=device, **w)

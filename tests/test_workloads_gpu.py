@@ -52,6 +52,19 @@ def test_decode_workload(name):
     assert_lse_close(got_lse, ref_lse, what=name)
 
 
+def test_tiered_workload():
+    g = si.make_workload("tiered_int8_decode", device="cuda")
+    lse = torch.empty((g.batch, g.n_heads), dtype=torch.float32, device="cuda")
+    out = attn.decode_tiered(g, lse_out=lse)
+    torch.cuda.synchronize()
+    rows = _sample_rows(g.batch, g.n_heads, 24, seed=8)
+    ref, ref_lse = oracle.decode_tiered(g.to("cpu"), rows=rows)
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    assert_close(np.stack([o[b, h] for b, h in rows]), ref, int8=True, what="tiered_int8_decode")
+    assert_lse_close(np.array([l[b, h] for b, h in rows]), ref_lse, what="tiered_int8_decode")
+
+
 @pytest.mark.parametrize("name", ["vision_2304", "swa_softcap_prefill"])
 def test_prefill_workload(name):
     g = si.make_workload(name, device="cuda")
