@@ -97,6 +97,7 @@ struct DecArgs {
     float* ws_fix_o;
     int B, Hq, Hkv, G, HG, U, n_hb, nh_box, split, cap_eff, window, P, R, max_pages, n_pages, paged;
     int ring;          // > 0: contiguous ring cache, logical token t in row t % ring
+    int logR;          // log2(R): rows per box are a power of two (a tile or a page)
     // tiered decode: kTierCold reads kv_len = cold lengths (window counted from the
     // newest hot token), kTierHot the hot ring (hot_len, hot_start); kTierPlain alone
     int tier;
@@ -524,7 +525,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                         for (int dist = LPK >> (C::LOG_GH + 1); dist >= 1; dist >>= 1)
                             acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], dist);
                         t = static_cast<float>(acc[0]) * inv_qs[0] *
-                            __half2float(kst[(key / A.R) * (sbb / 2) + sc_off + (key % A.R)]);
+                            __half2float(kst[(key >> A.logR) * (sbb / 2) + sc_off + (key & (A.R - 1))]);
                     } else {
                         float2 kx[E / 2];
                         load_row_slice<D, I8, GH>(kt + (key * A.nh_box + hl) * C::RB, c, kx);
@@ -581,7 +582,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     if (I8) {
                         const int key = st * C::KPS + kk;
                         const bool valid = key >= v_lo && key < v_hi;
-                        pv[st] = valid ? p * __half2float(vst[(key / A.R) * (sbb / 2) + sc_off + (key % A.R)]) : 0.f;
+                        pv[st] = valid ? p * __half2float(vst[(key >> A.logR) * (sbb / 2) + sc_off + (key & (A.R - 1))]) : 0.f;
                     }
                 }
 #pragma unroll
@@ -849,6 +850,8 @@ DecArgs make_dec_args(const DecodeLaunch& L, const DecodePlan& plan, int R) {
     a.window = L.window;
     a.P = paged ? L.page_size : 0;
     a.R = R;
+    a.logR = 0;
+    while ((1 << a.logR) < R) ++a.logR;
     a.max_pages = L.max_pages;
     a.n_pages = paged ? L.n_pages : 0;
     a.paged = paged;
