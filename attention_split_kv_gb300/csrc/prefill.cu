@@ -41,6 +41,8 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 // accumulators; otherwise logits are scaled (and capped) first.
 enum : int { kModeRaw = 0, kModeScaled = 1, kModeCapped = 2 };
 
+constexpr int BN_OF(int D) { return (D == 64) ? 128 : 64; }
+
 template <int D>
 struct PrefillCfg {
     static constexpr int NCH = D / 64;                   // 64-element (128-byte) chunks of D
@@ -50,11 +52,16 @@ struct PrefillCfg {
     // D=64/128: two full warpgroups, so that setmaxnreg can move registers
     // from the producer/MMA warpgroup (warps 4-7, two of them idle) to the
     // softmax warpgroup: 2 CTAs x 256 threads x 128 registers at launch, then
-    // 128 x 200 + 128 x 56 per CTA.  D=256 (one CTA per SM) runs 6 warps.
-    static constexpr int THREADS = (D <= 128) ? 256 : 192;
+    // 128 x 200 + 128 x 56 per CTA.  D=256 (one CTA per SM) runs two softmax
+    // warpgroups that split each row's keys in halves (so every SMSP has two
+    // softmax warps), then the producer and MMA warps: 10 warps.
+    static constexpr int NSM = (D == 256) ? 8 : 4;       // softmax warps
+    static constexpr int THREADS = (D <= 128) ? 256 : (NSM + 2) * 32;
+    static constexpr int PROD_WARP = NSM, MMA_WARP = NSM + 1;
+    static constexpr int CW = BN_OF(D) / (NSM / 4);      // S columns per softmax thread
     static constexpr int REG_SOFTMAX = 200, REG_OTHER = 56;
     static_assert(THREADS != 256 || (REG_SOFTMAX + REG_OTHER) * 128 * CTAS_PER_SM == 65536, "register split");
-    static constexpr int BN = (D == 64) ? 128 : 64;      // keys per tile
+    static constexpr int BN = BN_OF(D);                  // keys per tile
     // S and P buffers in TMEM.  D=64/128 (two CTAs per SM, 256 columns each)
     // keep one of each (D=64: S 128 + O 64 + P 64; D=128 with 64-key tiles:
     // S 64 + O 128 + P 32): the softmax frees S as soon as its row is in
@@ -77,7 +84,9 @@ struct PrefillCfg {
     // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], pv_done[2],
     // teardown, s_free.  K stages are released after their QK^T MMA and V stages after
     // their PV MMA, so the next K tiles load while the softmax still runs.
-    static constexpr int N_BARS = 1 + 4 * STAGES + 6 + 1 + 1;
+    // then, for split rows, x_full[4 quarters][2 parities]: the two halves of a
+    // row exchange their partial maxima through TMEM columns COL_X..
+    static constexpr int N_BARS = 1 + 4 * STAGES + 6 + 1 + 1 + 8;
     static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // slack for 1024-byte alignment
@@ -86,8 +95,10 @@ struct PrefillCfg {
     static constexpr uint32_t COL_P = COL_O + D;
     static constexpr uint32_t P_COLS = BN / 2;
     static constexpr uint32_t TMEM_COLS = (CTAS_PER_SM == 2) ? 256 : 512;
+    static constexpr uint32_t COL_X = COL_P + NBUF * P_COLS;   // split rows: 4 max slots + 2 sum slots
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-    static_assert(COL_P + NBUF * P_COLS <= TMEM_COLS, "TMEM budget");
+    static_assert(COL_P + NBUF * P_COLS + (NSM == 8 ? 6 : 0) <= TMEM_COLS, "TMEM budget");
+    static_assert(NSM == 4 || CTAS_PER_SM == 1, "split rows need one CTA per SM");
     // at most CTAS_PER_SM CTAs fit in an SM's 228 KB (1 KB reserved per CTA),
     // and together they never ask for more than the SM's 512 TMEM columns, so
     // no tcgen05.alloc waits on another CTA
@@ -200,6 +211,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int B_SFULL = 1 + 4 * STAGES, B_PFULL = B_SFULL + 2, B_PVDONE = B_SFULL + 4;
     const int B_TEARDOWN = B_SFULL + 6;
     const int B_SFREE = B_SFULL + 7;     // softmax has S in registers (single S buffer only)
+    const int B_XFULL = B_SFULL + 8;     // split rows: [quarter][parity], 64 arrivals each
     constexpr int NBUF = C::NBUF;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -282,15 +294,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_SFULL + b), 1);
-            mbar_init(bar(B_PFULL + b), 4 * 32);
+            mbar_init(bar(B_PFULL + b), C::NSM * 32);
             mbar_init(bar(B_PVDONE + b), 1);
         }
         mbar_init(bar(B_TEARDOWN), 1);
-        mbar_init(bar(B_SFREE), 4 * 32);
+        mbar_init(bar(B_SFREE), C::NSM * 32);
+        for (int x = 0; x < 8; ++x) mbar_init(bar(B_XFULL + x), 64);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == C::MMA_WARP) {
         tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -299,10 +312,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp >= 4) {
+    if (warp >= C::NSM) {
         // (setmaxnreg is executed by all four warps of a warpgroup)
         if constexpr (C::THREADS == 256) setmaxnreg_dec<C::REG_OTHER>();
-        if (warp == 4) {
+        if (warp == C::PROD_WARP) {
             // ------------------------------------------------------------ TMA producer
             // Contiguous: lane 0 loads Q and the K tiles, lane 1 the V tiles.  Paged:
             // lanes 0-15 load K and lanes 16-31 V, lane i of a group the box of the
@@ -382,7 +395,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         mbar_wait(bar(b_full + (j % NST)), (j / NST) & 1, &never, args.err, kErrTimeoutLoad);
                 }
             }
-        } else if (warp == 5) {
+        } else if (warp == C::MMA_WARP) {
             // ------------------------------------------------------------ MMA issuer
             if (lane == 0) {
                 constexpr uint32_t idesc_s = idesc_f16_f32(BM, BN, false);
@@ -445,10 +458,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else {
         // ------------------------------------------------------------ softmax warps
         if constexpr (C::THREADS == 256) setmaxnreg_inc<C::REG_SOFTMAX>();
-        const int row = threadIdx.x;           // 0..127 == TMEM lane
+        // split rows (D=256): warps w and w+4 share the TMEM lanes of quarter w%4
+        // and take the first / second half of each tile's keys and of O's columns
+        constexpr bool SPLIT = C::NSM == 8;
+        constexpr int CW = C::CW;              // S columns of this thread
+        constexpr int OW = D / (C::NSM / 4);   // O columns of this thread
+        const int quarter = warp & 3;
+        const int ch = SPLIT ? (warp >> 2) : 0;
+        const int row = quarter * 32 + lane;   // 0..127 == TMEM lane
         const int qi = q0 + row;             // query index within the sequence
         const int pos = pos0 + qi;           // its position among the keys
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        // split rows: hand this thread's value to the other half of its row and
+        // take that half's (through TMEM column slot `col`), on the quarter's
+        // exchange barrier of parity k & 1; false if the wait gave up
+        auto exchange = [&](float mine, uint32_t col, int k, float& other) -> bool {
+            tc_st_32x32b_x1(lane_base + C::COL_X + col + ch, __float_as_uint(mine));
+            tc_wait_st();
+            tc_fence_before();
+            const int xb = B_XFULL + quarter * 2 + (k & 1);
+            mbar_arrive(bar(xb));
+            if (!mbar_wait(bar(xb), (k >> 1) & 1, abort_flag, args.err, kErrTimeoutSoftmax)) return false;
+            tc_fence_after();
+            other = __uint_as_float(tc_ld_32x32b_x1(lane_base + C::COL_X + col + (ch ^ 1)));
+            tc_wait_ld();
+            return true;
+        };
         const float scale_log2 = args.scale * kLog2e;
         const float cap_log2 = args.softcap * kLog2e;
         const float inv_cap_scale = MODE == kModeCapped ? args.scale / args.softcap : 0.f;
@@ -458,15 +493,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int j = 0; j < n_tiles && ok; ++j) {
             if (!mbar_wait(bar(B_SFULL + (j % NBUF)), (j / NBUF) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
             tc_fence_after();
-            float t[BN];
+            float t[CW];
             {
-                uint32_t r[BN];
+                uint32_t r[CW];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-                    tc_ld_32x32b_x32(lane_base + (j % NBUF) * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
+                for (int c = 0; c < CW / 32; ++c)
+                    tc_ld_32x32b_x32(lane_base + (j % NBUF) * BN + ch * CW + c * 32,
+                                     *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
                 tc_wait_ld();
 #pragma unroll
-                for (int i = 0; i < BN; ++i) t[i] = __uint_as_float(r[i]);
+                for (int i = 0; i < CW; ++i) t[i] = __uint_as_float(r[i]);
             }
             const int key0 = (jt0 + j) * BN;
             const int key_last = key0 + BN - 1;
@@ -482,7 +518,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const float2 cl2 = make_float2(cap_log2, cap_log2);
                 bool big = false;
 #pragma unroll
-                for (int i = 0; i < BN; i += 2) {
+                for (int i = 0; i < CW; i += 2) {
                     const float2 x = fmul2(make_float2(t[i], t[i + 1]), ics);
                     big |= fabsf(x.x) > 0.25f || fabsf(x.y) > 0.25f;
                     const float2 y = fmul2(x, x);
@@ -496,18 +532,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     t[i + 1] = r.y;
                 }
                 if (__any_sync(0xffffffffu, big)) {
-                    uint32_t r[BN];
+                    uint32_t r[CW];
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c)
-                        tc_ld_32x32b_x32(lane_base + (j % NBUF) * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
+                    for (int c = 0; c < CW / 32; ++c)
+                        tc_ld_32x32b_x32(lane_base + (j % NBUF) * BN + ch * CW + c * 32,
+                                         *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
                     tc_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < BN; ++i)
+                    for (int i = 0; i < CW; ++i)
                         t[i] = cap_log2 * tanh_abs_accurate(__uint_as_float(r[i]) * inv_cap_scale);
                 }
             } else if constexpr (MODE == kModeScaled) {
 #pragma unroll
-                for (int i = 0; i < BN; ++i) t[i] *= scale_log2;
+                for (int i = 0; i < CW; ++i) t[i] *= scale_log2;
             }
             if constexpr (NBUF == 1) {
                 // S_j is in registers: the MMA warp may write S_{j+1}
@@ -516,8 +553,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             if (!full) {
 #pragma unroll
-                for (int i = 0; i < BN; ++i) {
-                    const int kj = key0 + i;
+                for (int i = 0; i < CW; ++i) {
+                    const int kj = key0 + ch * CW + i;
                     bool keep = kj < L;
                     if (args.causal) keep = keep && kj <= pos;
                     if (W > 0) {
@@ -528,7 +565,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (!keep) t[i] = -INFINITY;
                 }
             }
-            const float mx = row_max(t);
+            float mx = row_max(t);
+            if constexpr (SPLIT) {
+                float other;
+                if (!exchange(mx, 2 * (j & 1), j, other)) { ok = false; break; }
+                mx = fmaxf(mx, other);
+            }
             const float m_tile = MODE == kModeRaw ? mx * scale_log2 : mx;
             const bool need = m_tile > m_used + kRescaleThreshold || (m_used == -INFINITY && m_tile > -INFINITY);
             // the warp rescales O (below, once t[] is no longer live) if any of its rows moved its max
@@ -549,10 +591,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             make_float2(0.f, 0.f)};   // independent partial sums (short dependency chains)
             const float2 sl2 = make_float2(scale_log2, scale_log2);
             const float2 nm2 = make_float2(-m_off, -m_off);
-            const uint32_t p_addr = lane_base + C::COL_P + (j % NBUF) * C::P_COLS;
+            const uint32_t p_addr = lane_base + C::COL_P + (j % NBUF) * C::P_COLS + ch * (CW / 2);
             // 32 elements at a time, each chunk stored to TMEM as soon as it is packed
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < CW / 32; ++c) {
                 uint32_t packed[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
@@ -574,13 +616,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     !mbar_wait(bar(B_PVDONE + ((j - 1) % NBUF)), ((j - 1) / NBUF) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < OW / 32; ++c) {
                     uint32_t r[32];
-                    tc_ld_32x32b_x32(lane_base + C::COL_O + c * 32, r);
+                    tc_ld_32x32b_x32(lane_base + C::COL_O + ch * OW + c * 32, r);
                     tc_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_o);
-                    tc_st_32x32b_x32(lane_base + C::COL_O + c * 32, r);
+                    tc_st_32x32b_x32(lane_base + C::COL_O + ch * OW + c * 32, r);
                 }
             }
             if constexpr (PAGED) {
@@ -595,7 +637,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const int r0 = max(L - key0, 0);
                     const int per_chunk = (BN - r0) * 8;          // 16-byte units per chunk
                     uint8_t* vt = smem + C::OFF_V + stv * C::KV_BYTES;
-                    for (int u = row; u < NCH * per_chunk; u += BM) {
+                    for (int u = ch * BM + row; u < NCH * per_chunk; u += C::NSM * 32) {
                         const int c = u / per_chunk, rem = u - c * per_chunk;
                         *reinterpret_cast<uint4*>(vt + c * C::KV_CHUNK + (r0 + rem / 8) * 128 + (rem % 8) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
@@ -612,6 +654,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int jl = n_tiles - 1;
             ok = mbar_wait(bar(B_PVDONE + (jl % NBUF)), (jl / NBUF) & 1, abort_flag, args.err, kErrTimeoutMma);
         }
+        if constexpr (SPLIT) {
+            // the row sum is the two halves' sums
+            float other = 0.f;
+            if (ok) ok = exchange(l_sum, 4, n_tiles, other);
+            l_sum += other;
+        }
         if (ok) {
             tc_fence_after();
             const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
@@ -619,10 +667,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const bool row_ok = qi < n_q && q_base + qi >= 0 && q_base + qi < args.total_q;
             __half* orow = args.out + (static_cast<size_t>(q_base + qi) * args.Hq + h) * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < OW / 32; ++c) {
                 uint32_t r[32];
                 if (n_tiles > 0) {
-                    tc_ld_32x32b_x32(lane_base + C::COL_O + c * 32, r);
+                    tc_ld_32x32b_x32(lane_base + C::COL_O + ch * OW + c * 32, r);
                     tc_wait_ld();
                 } else {
 #pragma unroll
@@ -636,12 +684,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                                              __uint_as_float(r[2 * i + 1]) * inv_l);
                         hv[i] = *reinterpret_cast<const uint32_t*>(&p2);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + ch * OW + c * 32);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
                 }
             }
-            if (args.lse && row_ok) {
+            if (args.lse && row_ok && ch == 0) {
                 args.lse[static_cast<size_t>(q_base + qi) * args.Hq + h] =
                     l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
             }
@@ -649,7 +697,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == C::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
