@@ -50,7 +50,7 @@ def _load():
             i32, i64, f64 = ctypes.c_int, ctypes.c_long, ctypes.c_double
             lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_f16_to_double.restype = f64
-            lib.oracle_decode.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i64, i64,
+            lib.oracle_decode.argtypes = [P, i32, P, P, i32, P, P, P, P, i32, i32, i64, i64,
                                           i32, i32, i32, i32, i32, f64, f64,
                                           i32, P, P, P, P, i32, i32]
             lib.oracle_decode.restype = i32
@@ -60,7 +60,7 @@ def _load():
             lib.oracle_prefill_paged.argtypes = [P, P, P, P, P, P, i32, i32, i64, i32, i32, i32, i32,
                                                  i32, f64, f64, i32, P, P, P, P, i32]
             lib.oracle_prefill_paged.restype = i32
-            lib.oracle_decode_tiered.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i64, i64,
+            lib.oracle_decode_tiered.argtypes = [P, i32, P, P, i32, P, P, P, P, i32, i32, i64, i64,
                                                  P, P, P, P, i64,
                                                  i32, i32, i32, i32, i32, f64, f64,
                                                  i32, P, P, P, P, i32]
@@ -91,6 +91,14 @@ def _f16_bits(a):
     return a
 
 
+def _q_arg(q):
+    """(array, q_f32): f16 queries as their bits, f32 queries as binary32 values."""
+    a = _np(q)
+    if a.dtype == np.float32:
+        return a, 1
+    return _f16_bits(a), 0
+
+
 def f16_to_double(bits: int) -> float:
     return float(_load().oracle_f16_to_double(int(bits) & 0xFFFF))
 
@@ -106,7 +114,7 @@ def decode(case, rows=None, n_threads: int = 0):
     Returns (out float64 [n, D], lse float64 [n]) with lse in natural-log units.
     """
     lib = _load()
-    q = _f16_bits(case.q)
+    q, q_f32 = _q_arg(case.q)
     if case.int8:
         k = _np(case.k).astype(np.int8, copy=False)
         v = _np(case.v).astype(np.int8, copy=False)
@@ -126,7 +134,7 @@ def decode(case, rows=None, n_threads: int = 0):
     out = np.zeros((n, case.head_dim), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     n_pages = int(case.k.shape[0]) if pt is not None else 0
-    rc = lib.oracle_decode(_ptr(q), _ptr(k), _ptr(v), int(bool(case.int8)), _ptr(ks), _ptr(vs),
+    rc = lib.oracle_decode(_ptr(q), q_f32, _ptr(k), _ptr(v), int(bool(case.int8)), _ptr(ks), _ptr(vs),
                            _ptr(kv_len), _ptr(pt), int(case.page_size or 0),
                            int(case.max_pages or 0), int(case.cap), n_pages,
                            case.batch, case.n_heads, case.n_kv_heads, case.head_dim,
@@ -202,7 +210,7 @@ def decode_tiered(case, rows=None, n_threads: int = 0):
     Returns (out float64 [n, D], lse float64 [n]) with lse in natural-log units.
     """
     lib = _load()
-    q = _f16_bits(case.q)
+    q, q_f32 = _q_arg(case.q)
     if case.int8:
         ck = _np(case.k).astype(np.int8, copy=False)
         cv = _np(case.v).astype(np.int8, copy=False)
@@ -225,7 +233,7 @@ def decode_tiered(case, rows=None, n_threads: int = 0):
     out = np.zeros((n, case.head_dim), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     n_pages = int(case.k.shape[0]) if case.page_table is not None else 0
-    rc = lib.oracle_decode_tiered(_ptr(q), _ptr(ck), _ptr(cv), int(case.int8), _ptr(cks), _ptr(cvs),
+    rc = lib.oracle_decode_tiered(_ptr(q), q_f32, _ptr(ck), _ptr(cv), int(case.int8), _ptr(cks), _ptr(cvs),
                                   _ptr(cold_len), _ptr(pt), int(case.page_size), int(case.max_pages or 0),
                                   int(case.cap), n_pages, _ptr(hk), _ptr(hv), _ptr(hot_len), _ptr(hot_start),
                                   int(case.hot_ring), case.batch, case.n_heads, case.n_kv_heads, case.head_dim,

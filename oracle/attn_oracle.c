@@ -122,6 +122,15 @@ static void oracle_attend(const double* q, const double* K, const double* V,
     free(s);
 }
 
+/* One query element: q is f16 bits, or binary32 values when q_f32 (the f32-Q
+ * variant: attention.js executeAttentionTieredQuant requires f32 Q; a float
+ * widens to double exactly). */
+static double oracle_q_value(const void* q, int q_f32, long idx)
+{
+    if (q_f32) return (double)((const float*)q)[idx];
+    return oracle_f16_to_double(((const uint16_t*)q)[idx]);
+}
+
 /* One cache element (token t of sequence b, kv head g, dim d) as double. */
 static double oracle_cache_value(const void* cache, const uint16_t* scales, int is_int8,
                                  const int32_t* page_table, int P, int max_pages, long cap,
@@ -146,7 +155,8 @@ static double oracle_cache_value(const void* cache, const uint16_t* scales, int 
 }
 
 /*
- * Decode: one new query per sequence, at position kv_len[b]-1.
+ * Decode: one new query per sequence, at position kv_len[b]-1.  q [B][Hq][D]:
+ * f16 bits, or binary32 when q_f32.
  * rows: n_rows (b, h) pairs to evaluate (rows_b/rows_h), or n_rows < 0 for all
  * B*Hq in (b, h) row-major order.  out: [n][D], lse: [n].
  * ring > 0: the cache is a ring of `ring` slots per sequence (doppler run.js,
@@ -156,7 +166,7 @@ static double oracle_cache_value(const void* cache, const uint16_t* scales, int 
  * clamped), and the kept keys are the last min(kv_len, ring, window) tokens.
  * Returns 0, or -1 on an invalid argument.
  */
-int oracle_decode(const uint16_t* q, const void* k, const void* v, int kv_int8,
+int oracle_decode(const void* q, int q_f32, const void* k, const void* v, int kv_int8,
                   const uint16_t* k_scales, const uint16_t* v_scales,
                   const int32_t* kv_len, const int32_t* page_table,
                   int page_size, int max_pages, long cap, long n_pages,
@@ -189,7 +199,7 @@ int oracle_decode(const uint16_t* q, const void* k, const void* v, int kv_int8,
             double* Kd = (double*)malloc(sizeof(double) * (size_t)(keep > 0 ? keep : 1) * D);
             double* Vd = (double*)malloc(sizeof(double) * (size_t)(keep > 0 ? keep : 1) * D);
             for (int d = 0; d < D; ++d)
-                qd[d] = oracle_f16_to_double(q[((long)b * Hq + h) * D + d]);
+                qd[d] = oracle_q_value(q, q_f32, ((long)b * Hq + h) * D + d);
             for (long t = 0; t < keep; ++t)
                 for (int d = 0; d < D; ++d) {
                     long slot = (t0 + t) % ring;
@@ -206,7 +216,7 @@ int oracle_decode(const uint16_t* q, const void* k, const void* v, int kv_int8,
         double* Kd = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);
         double* Vd = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);
         for (int d = 0; d < D; ++d)
-            qd[d] = oracle_f16_to_double(q[((long)b * Hq + h) * D + d]);
+            qd[d] = oracle_q_value(q, q_f32, ((long)b * Hq + h) * D + d);
         for (long t = 0; t < L; ++t)
             for (int d = 0; d < D; ++d) {
                 Kd[t * D + d] = oracle_cache_value(k, k_scales, kv_int8, page_table, page_size,
@@ -239,7 +249,7 @@ int oracle_decode(const uint16_t* q, const void* k, const void* v, int kv_int8,
  * (overwritten hot tokens), so the window is applied by position here and
  * the kept keys are then attended without further masking.
  */
-int oracle_decode_tiered(const uint16_t* q,
+int oracle_decode_tiered(const void* q, int q_f32,
                          const void* ck, const void* cv, int cold_int8,
                          const uint16_t* ck_scales, const uint16_t* cv_scales,
                          const int32_t* cold_len, const int32_t* page_table,
@@ -275,7 +285,7 @@ int oracle_decode_tiered(const uint16_t* q,
         double* Kd = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1) * D);
         double* Vd = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1) * D);
         for (int d = 0; d < D; ++d)
-            qd[d] = oracle_f16_to_double(q[((long)b * Hq + h) * D + d]);
+            qd[d] = oracle_q_value(q, q_f32, ((long)b * Hq + h) * D + d);
         long kept = 0;
         for (long j = 0; j < Lc; ++j) {
             if (window > 0 && qpos - j >= window) continue;

@@ -68,6 +68,11 @@ def f16_normal(shape, seed: int, device: str = "cpu", chunk: int = 1 << 26) -> t
     return out
 
 
+def f32_normal(shape, seed: int, device: str = "cpu") -> torch.Tensor:
+    """N(0,1) float32 tensor drawn from a seeded generator (queries of the f32-Q variant)."""
+    return torch.randn(shape, generator=_gen(seed, device), device=device, dtype=torch.float32)
+
+
 def quantize_int8_rows(x: torch.Tensor, chunk_rows: int = 1 << 20):
     """Encode f16 rows (last dim) as symmetric int8 with one f16 scale per row.
 
@@ -243,7 +248,7 @@ def make_decode_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int,
                      lens, seed: int, *, cap: Optional[int] = None, int8: bool = False,
                      page_size: int = 0, n_pages: Optional[int] = None,
                      window: int = 0, softcap: float = 0.0, scale: Optional[float] = None,
-                     ring: int = 0, device: str = "cpu") -> DecodeCase:
+                     ring: int = 0, q_f32: bool = False, device: str = "cpu") -> DecodeCase:
     """Build a decode case.
 
     ``lens`` is a list of per-sequence KV lengths, or a (lo, hi) tuple for
@@ -252,7 +257,8 @@ def make_decode_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int,
     seeded permutation assigning pages to sequences.  With ``ring > 0`` the cache
     is a ring of ``ring`` slots per sequence, drawn directly (every slot holds
     N(0,1) values, as a ring does once its sequence has passed ``ring`` tokens);
-    ``lens`` are then logical lengths and may exceed ``ring``.
+    ``lens`` are then logical lengths and may exceed ``ring``.  ``q_f32`` draws the
+    queries in float32 (not rounded to f16).
     """
     if isinstance(lens, tuple):
         lens = _lengths(batch, lens[0], lens[1], seed)
@@ -260,7 +266,7 @@ def make_decode_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int,
     assert len(lens) == batch
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
-    q = f16_normal((batch, n_heads, head_dim), seed * 1000 + 1, device)
+    q = (f32_normal if q_f32 else f16_normal)((batch, n_heads, head_dim), seed * 1000 + 1, device)
     kv_len = torch.tensor(lens, dtype=torch.int32, device=device)
     if ring > 0:
         assert page_size <= 0
@@ -345,7 +351,8 @@ def ring_from_contiguous(case: DecodeCase, ring: int) -> DecodeCase:
 def make_tiered_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int, cold_lens, hot_lens,
                      hot_ring: int, seed: int, *, hot_starts=None, int8: bool = False, page_size: int = 0,
                      n_pages: Optional[int] = None, cap: Optional[int] = None, window: int = 0,
-                     softcap: float = 0.0, scale: Optional[float] = None, device: str = "cpu") -> TieredCase:
+                     softcap: float = 0.0, scale: Optional[float] = None, q_f32: bool = False,
+                     device: str = "cpu") -> TieredCase:
     """Build a tiered decode case: the cold tier as make_decode_case builds a
     cache (``cold_lens`` tokens, contiguous or paged, f16 or int8) and an f16 hot
     ring of ``hot_ring`` slots holding N(0,1) values in every slot.  ``hot_lens``
@@ -353,7 +360,7 @@ def make_tiered_case(batch: int, n_heads: int, n_kv_heads: int, head_dim: int, c
     seeded slots in [0, hot_ring)."""
     cold = make_decode_case(batch, n_heads, n_kv_heads, head_dim, cold_lens, seed, cap=cap, int8=int8,
                             page_size=page_size, n_pages=n_pages, window=window, softcap=softcap,
-                            scale=scale, device=device)
+                            scale=scale, q_f32=q_f32, device=device)
     if isinstance(hot_lens, tuple):
         hot_lens = _lengths(batch, hot_lens[0], hot_lens[1], seed * 7 + 3)
     hot_lens = [int(x) for x in hot_lens]

@@ -604,3 +604,34 @@ def test_tiered_equals_one_contiguous_cache_of_both_tiers(window):
     b, lb = oracle.decode(flat)
     np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
     np.testing.assert_allclose(la, lb, rtol=0, atol=1e-13)
+
+
+# ---- f32 queries --------------------------------------------------------------
+
+def test_f32_queries_that_are_f16_values_match_the_f16_path():
+    # a binary32 query holding exactly the f16 values is the same query
+    c = si.make_decode_case(3, 4, 2, 32, [1, 40, 77], seed=71, int8=True, page_size=16, window=30)
+    c32 = si.DecodeCase(**{**c.__dict__, "q": c.q.float()})
+    a, la = oracle.decode(c)
+    b, lb = oracle.decode(c32)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+    t = si.make_tiered_case(2, 4, 2, 16, [10, 30], [5, 40], 16, seed=72)
+    t32 = si.TieredCase(**{**t.__dict__, "q": t.q.float()})
+    a, la = oracle.decode_tiered(t)
+    b, lb = oracle.decode_tiered(t32)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+def test_f32_queries_match_brute_force():
+    c = si.make_decode_case(2, 4, 2, 16, [9, 33], seed=73, q_f32=True, softcap=10.0)
+    assert c.q.dtype == torch.float32 and not torch.equal(c.q, c.q.half().float())
+    got, lse = oracle.decode(c)
+    for b, L in enumerate([9, 33]):
+        K = c.k[b, :L].double().numpy()
+        V = c.v[b, :L].double().numpy()
+        for h in range(4):
+            s = c.scale * (K[:, h // 2] @ c.q[b, h].double().numpy())
+            s = 10.0 * np.tanh(s / 10.0)
+            p = scipy.special.softmax(s)
+            np.testing.assert_allclose(got[b * 4 + h], p @ V[:, h // 2], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[b * 4 + h], scipy.special.logsumexp(s), rtol=0, atol=1e-12)
