@@ -16,16 +16,17 @@ from typing import Optional
 
 __all__ = [
     "ATTN_OK", "ATTN_EINVAL", "ATTN_EUNSUPPORTED", "ATTN_ECUDA", "ATTN_EBOUNDS", "ATTN_ETIMEOUT",
-    "ATTN_KV_F16", "ATTN_KV_INT8", "AttnError", "AttnLibraryMissing",
+    "ATTN_KV_F16", "ATTN_KV_INT8", "ATTN_F16", "ATTN_F32", "AttnError", "AttnLibraryMissing",
     "lib_path", "load", "build", "exported_symbols",
     "attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-    "attn_decode_ring", "attn_decode_tiered", "attn_decode_tiered_workspace_size", "attn_decode_noalloc",
-    "attn_prefill", "attn_prefill_paged", "attn_decode_validate", "attn_device_status",
+    "attn_decode_ring", "attn_decode_ex", "attn_decode_tiered", "attn_decode_tiered_workspace_size",
+    "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate", "attn_device_status",
     "decode", "decode_tiered", "prefill", "prefill_paged",
 ]
 
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_EBOUNDS, ATTN_ETIMEOUT = range(6)
 ATTN_KV_F16, ATTN_KV_INT8 = 0, 1
+ATTN_F16, ATTN_F32 = 0, 1
 _STATUS = {0: "ATTN_OK", 1: "ATTN_EINVAL", 2: "ATTN_EUNSUPPORTED", 3: "ATTN_ECUDA", 4: "ATTN_EBOUNDS",
            5: "ATTN_ETIMEOUT"}
 
@@ -35,7 +36,7 @@ _lib = None
 
 # every entry point include/attn.h declares
 exported_symbols = ("attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
-                    "attn_decode_ring", "attn_decode_tiered", "attn_decode_tiered_workspace_size",
+                    "attn_decode_ring", "attn_decode_ex", "attn_decode_tiered", "attn_decode_tiered_workspace_size",
                     "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate",
                     "attn_device_status")
 
@@ -78,8 +79,11 @@ def load():
     lib.attn_decode_ring.restype = I
     lib.attn_decode_tiered_workspace_size.argtypes = [I, I, I, I, I, I, I]
     lib.attn_decode_tiered_workspace_size.restype = SZ
-    lib.attn_decode_tiered.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, P, P, P, P, I, I, I, I, I, I, F, F, I,
-                                       P, P, P, SZ, P]
+    lib.attn_decode_tiered.argtypes = [P, I, P, P, P, P, I, P, P, I, I, I, I, P, P, P, P, I, I, I, I, I, I, F, F,
+                                       I, P, I, P, P, SZ, P]
+    lib.attn_decode_ex.argtypes = [P, I, P, P, P, P, I, I, I, I, I, P, P, I, I, I, I, I, I, F, F, I, P, I, P, P, SZ,
+                                   P]
+    lib.attn_decode_ex.restype = I
     lib.attn_decode_tiered.restype = I
     lib.attn_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, I, I, I, I, I, F, F, I, P, P, P]
     lib.attn_decode_noalloc.restype = I
@@ -156,36 +160,58 @@ def attn_decode_tiered_workspace_size(batch, n_heads, n_kv_heads, head_dim, cold
                                                         hot_ring, split_keys))
 
 
-def attn_decode_tiered(q, cold_k, cold_v, cold_k_scales, cold_v_scales, cold_dtype, cold_len, cold_page_table,
-                       cold_page_size, cold_max_pages_per_seq, cold_n_pages, cold_max_kv, hot_k, hot_v, hot_len,
-                       hot_start, hot_ring, batch, n_heads, n_kv_heads, head_dim, window, softcap, scale,
-                       split_keys, out, lse_out, workspace, workspace_bytes, stream=None) -> None:
-    _check(load().attn_decode_tiered(_ptr(q), _ptr(cold_k), _ptr(cold_v), _ptr(cold_k_scales), _ptr(cold_v_scales),
+def attn_decode_ex(q, q_dtype, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages, max_kv,
+                   ring_size, k_scales, v_scales, kv_dtype, batch, n_heads, n_kv_heads, head_dim, window, softcap,
+                   scale, split_keys, out, out_dtype, lse_out, workspace, workspace_bytes, stream=None) -> None:
+    _check(load().attn_decode_ex(_ptr(q), int(q_dtype), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(page_table),
+                                 int(page_size), int(max_pages_per_seq), int(n_pages), int(max_kv), int(ring_size),
+                                 _ptr(k_scales), _ptr(v_scales), int(kv_dtype), int(batch), int(n_heads),
+                                 int(n_kv_heads), int(head_dim), int(window), float(softcap), float(scale),
+                                 int(split_keys), _ptr(out), int(out_dtype), _ptr(lse_out), _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream)))
+
+
+def _dtype_of(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    raise AttnError(ATTN_EINVAL, "q and out must be float16 or float32, not %s" % t.dtype)
+
+
+def attn_decode_tiered(q, q_dtype, cold_k, cold_v, cold_k_scales, cold_v_scales, cold_dtype, cold_len,
+                       cold_page_table, cold_page_size, cold_max_pages_per_seq, cold_n_pages, cold_max_kv, hot_k,
+                       hot_v, hot_len, hot_start, hot_ring, batch, n_heads, n_kv_heads, head_dim, window, softcap,
+                       scale, split_keys, out, out_dtype, lse_out, workspace, workspace_bytes, stream=None) -> None:
+    _check(load().attn_decode_tiered(_ptr(q), int(q_dtype), _ptr(cold_k), _ptr(cold_v), _ptr(cold_k_scales),
+                                     _ptr(cold_v_scales),
                                      int(cold_dtype), _ptr(cold_len), _ptr(cold_page_table), int(cold_page_size),
                                      int(cold_max_pages_per_seq), int(cold_n_pages), int(cold_max_kv), _ptr(hot_k),
                                      _ptr(hot_v), _ptr(hot_len), _ptr(hot_start), int(hot_ring), int(batch),
                                      int(n_heads), int(n_kv_heads), int(head_dim), int(window), float(softcap),
-                                     float(scale), int(split_keys), _ptr(out), _ptr(lse_out), _ptr(workspace),
-                                     int(workspace_bytes), _stream(stream)))
+                                     float(scale), int(split_keys), _ptr(out), int(out_dtype), _ptr(lse_out),
+                                     _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
-def decode_tiered(case, out=None, lse_out=None, workspace=None, split_keys: int = 0, stream=None):
-    """attn_decode_tiered on a TieredCase-like object (tensors already on the GPU)."""
+def decode_tiered(case, out=None, lse_out=None, workspace=None, split_keys: int = 0, stream=None, out_f32=False):
+    """attn_decode_tiered on a TieredCase-like object (tensors already on the GPU);
+    q f16 or f32 as the case holds it, out f16 (or f32 with ``out_f32``)."""
     import torch
     dev = case.q.device
     B, Hq, Hkv, D = case.batch, case.n_heads, case.n_kv_heads, case.head_dim
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=torch.float16, device=dev)
+        out = torch.empty((B, Hq, D), dtype=torch.float32 if out_f32 else torch.float16, device=dev)
     ws_bytes = attn_decode_tiered_workspace_size(B, Hq, Hkv, D, case.cap, case.hot_ring, split_keys)
     if ws_bytes == 0:
         raise AttnError(ATTN_EINVAL, "invalid sizes for the tiered decode workspace")
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    attn_decode_tiered(case.q, case.k, case.v, case.k_scales, case.v_scales,
+    attn_decode_tiered(case.q, _dtype_of(case.q), case.k, case.v, case.k_scales, case.v_scales,
                        ATTN_KV_INT8 if case.int8 else ATTN_KV_F16, case.kv_len, case.page_table, case.page_size,
                        case.max_pages, case.n_pages, case.cap, case.hot_k, case.hot_v, case.hot_len,
                        case.hot_start, case.hot_ring, B, Hq, Hkv, D, case.window, case.softcap, case.scale,
-                       split_keys, out, lse_out, workspace, workspace.numel(), stream)
+                       split_keys, out, _dtype_of(out), lse_out, workspace, workspace.numel(), stream)
     return out
 
 
@@ -226,7 +252,7 @@ def attn_device_status(stream=None) -> int:
 
 # ---------------------------------------------------------------- conveniences
 def decode(case, out=None, lse_out=None, workspace=None, split_keys: int = 0, max_kv: Optional[int] = None,
-           stream=None):
+           stream=None, out_f32=False):
     """attn_decode on a DecodeCase-like object (tensors already on the GPU);
     attn_decode_ring when the case holds a ring cache (``case.ring > 0``).
 
@@ -239,12 +265,19 @@ def decode(case, out=None, lse_out=None, workspace=None, split_keys: int = 0, ma
     if max_kv is None:
         max_kv = ring if ring else case.cap
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=torch.float16, device=dev)
+        out = torch.empty((B, Hq, D), dtype=torch.float32 if out_f32 else torch.float16, device=dev)
     ws_bytes = attn_decode_workspace_size(B, Hq, Hkv, D, max_kv, split_keys)
     if ws_bytes == 0:
         raise AttnError(ATTN_EINVAL, "invalid sizes for the decode workspace")
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    qt, ot = _dtype_of(case.q), _dtype_of(out)
+    if qt != ATTN_F16 or ot != ATTN_F16:
+        attn_decode_ex(case.q, qt, case.k, case.v, case.kv_len, case.page_table, case.page_size, case.max_pages,
+                       case.n_pages, max_kv, ring, case.k_scales, case.v_scales,
+                       ATTN_KV_INT8 if case.int8 else ATTN_KV_F16, B, Hq, Hkv, D, case.window, case.softcap,
+                       case.scale, split_keys, out, ot, lse_out, workspace, workspace.numel(), stream)
+        return out
     if ring:
         attn_decode_ring(case.q, case.k, case.v, case.kv_len, ring, case.k_scales, case.v_scales,
                          ATTN_KV_INT8 if case.int8 else ATTN_KV_F16, B, Hq, Hkv, D, case.window, case.softcap,

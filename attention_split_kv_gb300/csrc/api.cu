@@ -183,7 +183,9 @@ static attn_status decode_prepare(const void* q, const void* k_cache, const void
                                   int max_kv, const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
                                   int batch, int n_heads, int n_kv_heads, int head_dim, int window, float softcap,
                                   float scale, int split_keys, void* out, float* lse_out, void* stream, int ring,
-                                  DecodeLaunch* Lp, DecodePlan* plan_p) {
+                                  attn_dtype q_dtype, attn_dtype out_dtype, DecodeLaunch* Lp, DecodePlan* plan_p) {
+    if ((q_dtype != ATTN_F16 && q_dtype != ATTN_F32) || (out_dtype != ATTN_F16 && out_dtype != ATTN_F32))
+        return set_error(ATTN_EINVAL, "attn_decode: q_dtype and out_dtype must be ATTN_F16 or ATTN_F32");
     if (!q || !k_cache || !v_cache || !kv_len || !out)
         return set_error(ATTN_EINVAL, "attn_decode: q, k_cache, v_cache, kv_len and out must be non-null");
     if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0)
@@ -248,6 +250,8 @@ static attn_status decode_prepare(const void* q, const void* k_cache, const void
     L.split_keys = split_keys;
     L.out = out;
     L.lse = lse_out;
+    L.q_f32 = q_dtype == ATTN_F32;
+    L.out_f32 = out_dtype == ATTN_F32;
     L.stream = static_cast<cudaStream_t>(stream);
     return ATTN_OK;
 }
@@ -266,12 +270,14 @@ static attn_status decode_entry(const void* q, const void* k_cache, const void* 
                                 int max_kv, const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
                                 int batch, int n_heads, int n_kv_heads, int head_dim, int window, float softcap,
                                 float scale, int split_keys, void* out, float* lse_out, void* workspace,
-                                size_t workspace_bytes, void* stream, int ring) {
+                                size_t workspace_bytes, void* stream, int ring, attn_dtype q_dtype = ATTN_F16,
+                                attn_dtype out_dtype = ATTN_F16) {
     DecodeLaunch L;
     DecodePlan plan;
     attn_status st = decode_prepare(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages,
                                     max_kv, k_scales, v_scales, kv_dtype, batch, n_heads, n_kv_heads, head_dim,
-                                    window, softcap, scale, split_keys, out, lse_out, stream, ring, &L, &plan);
+                                    window, softcap, scale, split_keys, out, lse_out, stream, ring, q_dtype,
+                                    out_dtype, &L, &plan);
     if (st != ATTN_OK) return st;
     if ((st = check_workspace("attn_decode", workspace, workspace_bytes, plan.bytes)) != ATTN_OK) return st;
     int* err = device_error_word();
@@ -303,14 +309,15 @@ size_t attn_decode_tiered_workspace_size(int batch, int n_heads, int n_kv_heads,
     return bytes;
 }
 
-attn_status attn_decode_tiered(const void* q, const void* cold_k, const void* cold_v, const void* cold_k_scales,
+attn_status attn_decode_tiered(const void* q, attn_dtype q_dtype, const void* cold_k, const void* cold_v,
+                               const void* cold_k_scales,
                                const void* cold_v_scales, attn_kv_dtype cold_dtype, const int32_t* cold_len,
                                const int32_t* cold_page_table, int cold_page_size, int cold_max_pages_per_seq,
                                int cold_n_pages, int cold_max_kv, const void* hot_k, const void* hot_v,
                                const int32_t* hot_len, const int32_t* hot_start, int hot_ring, int batch,
                                int n_heads, int n_kv_heads, int head_dim, int window, float softcap, float scale,
-                               int split_keys, void* out, float* lse_out, void* workspace, size_t workspace_bytes,
-                               void* stream) {
+                               int split_keys, void* out, attn_dtype out_dtype, float* lse_out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
     if (!hot_k || !hot_v || !hot_len || !hot_start)
         return set_error(ATTN_EINVAL, "attn_decode_tiered: hot_k, hot_v, hot_len and hot_start must be non-null");
     if (hot_ring < 16 || hot_ring % 16 != 0)
@@ -321,11 +328,11 @@ attn_status attn_decode_tiered(const void* q, const void* cold_k, const void* co
     attn_status st = decode_prepare(q, cold_k, cold_v, cold_len, cold_page_table, cold_page_size,
                                     cold_max_pages_per_seq, cold_n_pages, cold_max_kv, cold_k_scales, cold_v_scales,
                                     cold_dtype, batch, n_heads, n_kv_heads, head_dim, window, softcap, scale,
-                                    split_keys, out, lse_out, stream, 0, &Lc, &pc);
+                                    split_keys, out, lse_out, stream, 0, q_dtype, out_dtype, &Lc, &pc);
     if (st != ATTN_OK) return st;
     st = decode_prepare(q, hot_k, hot_v, hot_len, nullptr, 0, 0, 0, hot_ring, nullptr, nullptr, ATTN_KV_F16, batch,
                         n_heads, n_kv_heads, head_dim, window, softcap, scale, split_keys, out, lse_out, stream,
-                        hot_ring, &Lh, &ph);
+                        hot_ring, q_dtype, out_dtype, &Lh, &ph);
     if (st != ATTN_OK) return st;
     size_t hot_off = 0, bytes = 0;
     if (!tiered_plans(batch, n_heads, n_kv_heads, head_dim, cold_max_kv, hot_ring, split_keys, &pc, &ph, &hot_off,
@@ -358,6 +365,24 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
     return decode_entry(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages, max_kv,
                         k_scales, v_scales, kv_dtype, batch, n_heads, n_kv_heads, head_dim, window, softcap, scale,
                         split_keys, out, lse_out, workspace, workspace_bytes, stream, 0);
+}
+
+attn_status attn_decode_ex(const void* q, attn_dtype q_dtype, const void* k_cache, const void* v_cache,
+                           const int32_t* kv_len, const int32_t* page_table, int page_size, int max_pages_per_seq,
+                           int n_pages, int max_kv, int ring_size, const void* k_scales, const void* v_scales,
+                           attn_kv_dtype kv_dtype, int batch, int n_heads, int n_kv_heads, int head_dim, int window,
+                           float softcap, float scale, int split_keys, void* out, attn_dtype out_dtype,
+                           float* lse_out, void* workspace, size_t workspace_bytes, void* stream) {
+    if (ring_size != 0) {
+        if (ring_size < 16 || ring_size % 16 != 0)
+            return set_error(ATTN_EUNSUPPORTED, "attn_decode_ex: ring_size %d must be a positive multiple of 16",
+                             ring_size);
+        if (page_table) return set_error(ATTN_EINVAL, "attn_decode_ex: a ring cache takes no page table");
+        max_kv = ring_size;
+    }
+    return decode_entry(q, k_cache, v_cache, kv_len, page_table, page_size, max_pages_per_seq, n_pages, max_kv,
+                        k_scales, v_scales, kv_dtype, batch, n_heads, n_kv_heads, head_dim, window, softcap, scale,
+                        split_keys, out, lse_out, workspace, workspace_bytes, stream, ring_size, q_dtype, out_dtype);
 }
 
 attn_status attn_decode_ring(const void* q, const void* k_ring, const void* v_ring, const int32_t* seq_len,

@@ -84,6 +84,8 @@ struct DecodeLaunch {
     int tier = 0;
     const int32_t* hot_len = nullptr;
     const int32_t* hot_start = nullptr;
+    int q_f32 = 0;          // q is f32 [B, Hq, D] (else f16)
+    int out_f32 = 0;        // out is f32 [B, Hq, D] (else f16)
     void* out;
     float* lse;
     void* workspace;
@@ -101,7 +103,7 @@ struct DecodePlan {
     int split;         // keys per split (multiple of 16)
     long max_items;    // upper bound of work items (sequence, head block, split)
     int n_fix;         // fix-up slots: one per CTA of the balanced kernel (the most it may launch)
-    size_t off_tpref, off_fix_meta, off_lse, off_fix_lse, off_o, off_fix_o, bytes;
+    size_t off_tpref, off_fix_meta, off_lse, off_fix_lse, off_o, off_fix_o, off_qsplit, bytes;
 };
 bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys, DecodePlan* plan);
 attn_status launch_decode(const DecodeLaunch& L, const DecodePlan& plan);

@@ -84,6 +84,7 @@ struct DecCfg {
 
 struct DecArgs {
     const __half* q;
+    const float* q32;  // f32 queries (then q is unused by the CUDA-core kernel)
     const int32_t* kv_len;
     const int32_t* page_table;
     int32_t* ws_prefix;
@@ -418,13 +419,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
             for (int s = 0; s < GH; ++s) {
                 const int head = g * A.G + hg * GH + (s ^ rot);
-                const __half* qrow = A.q + ((size_t)I.b * A.Hq + head) * D;
+                const size_t qoff = ((size_t)I.b * A.Hq + head) * D;
 #pragma unroll
                 for (int v = 0; v < C::NV; ++v)
 #pragma unroll
                     for (int e = 0; e < C::EV; e += 2) {
                         const int dim = (v * LPK + c) * C::EV + e;
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(qrow + dim));
+                        const float2 f = A.q32 ? *reinterpret_cast<const float2*>(A.q32 + qoff + dim)
+                                               : __half22float2(*reinterpret_cast<const __half2*>(A.q + qoff + dim));
                         q2[s][(v * C::EV + e) / 2] = make_float2(f.x * A.qscale, f.y * A.qscale);
                     }
             }
@@ -653,6 +655,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
 #include "decode_tc.cuh"
 
+// f32 queries for the tensor-core kernel: q = hi + lo with hi = f16(q) and
+// lo = f16(q - hi) (RNE both), so hi + lo matches q to about 2^-22 of |q|;
+// hi goes to rows [0, B) of a [2B, Hq, D] f16 array and lo to rows [B, 2B).
+__global__ void q_split_kernel(const float* __restrict__ q, __half* __restrict__ hl, long n) {
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const float x = q[i];
+        const __half hi = __float2half_rn(x);
+        hl[i] = hi;
+        hl[n + i] = __float2half_rn(x - __half2float(hi));
+    }
+}
+
 // One tier of the combine: where a split kernel left its partials, and the
 // range arguments that say which items it wrote.
 struct CombTier {
@@ -674,9 +688,9 @@ struct CombTiers {
 
 // One warp per (sequence, query head): log-sum-exp merge of the splits of
 // every tier (one tier for a plain decode; cold and hot for a tiered decode).
-template <int D, int NT>
+template <int D, int NT, typename OutT>
 __global__ void __launch_bounds__(128)
-decode_combine_kernel(const CombTiers<NT> T, __half* __restrict__ out, float* __restrict__ lse_out, int B, int Hq,
+decode_combine_kernel(const CombTiers<NT> T, OutT* __restrict__ out, float* __restrict__ lse_out, int B, int Hq,
                       int G, int GH, int HG, int n_hb) {
     constexpr int DPL = D / 32;   // dims per lane
     // launched as a programmatic dependent of the split kernel: wait until that
@@ -809,9 +823,14 @@ decode_combine_kernel(const CombTiers<NT> T, __half* __restrict__ out, float* __
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
-    __half* dst = out + ((size_t)b * Hq + h) * D + lane * DPL;
+    OutT* dst = out + ((size_t)b * Hq + h) * D + lane * DPL;
 #pragma unroll
-    for (int i = 0; i < DPL; i += 2) *reinterpret_cast<__half2*>(dst + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
+    for (int i = 0; i < DPL; i += 2) {
+        if constexpr (sizeof(OutT) == 4)
+            *reinterpret_cast<float2*>(dst + i) = make_float2(acc[i] * inv, acc[i + 1] * inv);
+        else
+            *reinterpret_cast<__half2*>(dst + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
+    }
     if (lse_out && lane == 0)
         lse_out[(size_t)b * Hq + h] = wsum > 0.f ? (M + __log2f(wsum)) * 0.6931471805599453f : -INFINITY;
 }
@@ -821,7 +840,8 @@ DecArgs make_dec_args(const DecodeLaunch& L, const DecodePlan& plan, int R) {
     const bool paged = L.page_table != nullptr;
     const int cap_layout = paged ? L.max_pages * L.page_size : L.max_kv;
     DecArgs a;
-    a.q = static_cast<const __half*>(L.q);
+    a.q = L.q_f32 ? nullptr : static_cast<const __half*>(L.q);
+    a.q32 = L.q_f32 ? static_cast<const float*>(L.q) : nullptr;
     a.kv_len = L.kv_len;
     a.page_table = L.page_table;
     uint8_t* ws = static_cast<uint8_t*>(L.workspace);
@@ -909,8 +929,11 @@ attn_status launch_combine(const DecodeLaunch& L, const DecodePlan& plan, const 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, NT>, T, static_cast<__half*>(L.out), L.lse,
-                                       L.B, L.Hq, L.Hq / L.Hkv, plan.GH, plan.HG, plan.n_hb);
+    cudaError_t e = L.out_f32
+        ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, NT, float>, T, static_cast<float*>(L.out), L.lse, L.B,
+                             L.Hq, L.Hq / L.Hkv, plan.GH, plan.HG, plan.n_hb)
+        : cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, NT, __half>, T, static_cast<__half*>(L.out), L.lse, L.B,
+                             L.Hq, L.Hq / L.Hkv, plan.GH, plan.HG, plan.n_hb);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode combine launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
@@ -932,19 +955,30 @@ int decode_grid(const DecodePlan& plan) {
 }
 
 // Tensor-core split kernel: f16 caches, head_dim 64/128, boxes of 16 rows x NH heads.
-template <int D, int NH>
+// Q2: f32 queries, split into f16 hi and lo terms in the workspace first.
+template <int D, int NH, bool Q2>
 attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, SplitOut* so) {
-    using C = tcdec::Cfg<D>;
+    using C = tcdec::Cfg<D, Q2>;
     const bool paged = L.page_table != nullptr;
     CUtensorMap tq, tk, tv;
     attn_status st;
     const int q_rows = L.Hq < tcdec::QROWS ? L.Hq : tcdec::QROWS;
+    const void* qsrc = L.q;
+    if constexpr (Q2) {
+        __half* hl = reinterpret_cast<__half*>(static_cast<uint8_t*>(L.workspace) + plan.off_qsplit);
+        const long n = (long)L.B * L.Hq * D;
+        const int blocks = (int)((n + 255) / 256 < 4 * sm_count() ? (n + 255) / 256 : 4 * sm_count());
+        q_split_kernel<<<blocks, 256, 0, L.stream>>>(static_cast<const float*>(L.q), hl, n);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(ATTN_ECUDA, "q split launch failed: %s", cudaGetErrorString(e));
+        qsrc = hl;
+    }
     {
-        // q [B][Hq][D]: boxes of (64 dims, q_rows heads, 1), 128-byte swizzle
-        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)L.Hq, (uint64_t)L.B};
+        // q [B][Hq][D] (Q2: [2B][Hq][D], hi then lo): boxes of (64 dims, q_rows heads, 1), 128-byte swizzle
+        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)L.Hq, (uint64_t)L.B * (Q2 ? 2 : 1)};
         const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * L.Hq};
         const uint32_t box[3] = {64u, (uint32_t)q_rows, 1u};
-        if ((st = encode_tmap_sw128(&tq, L.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, dims, strides, box)) != ATTN_OK)
+        if ((st = encode_tmap_sw128(&tq, qsrc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, dims, strides, box)) != ATTN_OK)
             return st;
     }
     {
@@ -967,7 +1001,7 @@ attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, Spli
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(tcdec::decode_tc_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(tcdec::decode_tc_kernel<D, NH, Q2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_ALLOC) != cudaSuccess)
             return set_error(ATTN_ECUDA, "cudaFuncSetAttribute(decode tc smem) failed");
         attr_set[dev] = true;
@@ -975,7 +1009,7 @@ attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, Spli
     const DecArgs a = make_dec_args(L, plan, 16);
     // balanced: every CTA takes an equal share of the tiles (see decode_tc.cuh)
     const int grid = sm_count() < plan.n_fix ? sm_count() : plan.n_fix;
-    tcdec::decode_tc_kernel<D, NH><<<grid, tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a, q_rows);
+    tcdec::decode_tc_kernel<D, NH, Q2><<<grid, tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a, q_rows);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode tc launch failed: %s", cudaGetErrorString(e));
     so->a = a;
@@ -997,10 +1031,10 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan, Split
         while (nh < plan.nh_box) nh <<= 1;
         if ((!paged || L.page_size % 16 == 0) && nh <= L.Hkv && L.B <= tcdec::kMaxBatch) {
             switch (nh) {
-                case 1: return launch_decode_tc<D, 1>(L, plan, so);
-                case 2: return launch_decode_tc<D, 2>(L, plan, so);
-                case 4: return launch_decode_tc<D, 4>(L, plan, so);
-                default: return launch_decode_tc<D, 8>(L, plan, so);
+                case 1: return L.q_f32 ? launch_decode_tc<D, 1, true>(L, plan, so) : launch_decode_tc<D, 1, false>(L, plan, so);
+                case 2: return L.q_f32 ? launch_decode_tc<D, 2, true>(L, plan, so) : launch_decode_tc<D, 2, false>(L, plan, so);
+                case 4: return L.q_f32 ? launch_decode_tc<D, 4, true>(L, plan, so) : launch_decode_tc<D, 4, false>(L, plan, so);
+                default: return L.q_f32 ? launch_decode_tc<D, 8, true>(L, plan, so) : launch_decode_tc<D, 8, false>(L, plan, so);
             }
         }
     }
@@ -1122,7 +1156,10 @@ bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys,
     plan->off_o = off;
     off += up(rows * D * 4);
     plan->off_fix_o = off;
-    off += frows * D * 4;
+    off += up(frows * D * 4);
+    // f32 queries on the tensor-core kernel: their f16 hi and lo terms
+    plan->off_qsplit = off;
+    off += (size_t)2 * B * Hq * D * 2;
     plan->bytes = off;
     return true;
 }

@@ -40,12 +40,16 @@ constexpr int TR = 128;                       // rows of the K/V operand per MMA
 constexpr int QROWS = 32;                     // query rows written (NW units x up to 4 heads)
 constexpr int kMaxBatch = 2048;               // sequences per call (two prefixes live in shared memory)
 
-template <int D>
+// Q2: f32 queries, held as two f16 terms (q = hi + lo to 2^-22 relative): a
+// Q' chunk keeps hi in rows 0-31 and lo in rows 32-63, and every QK^T step
+// runs a second MMA on the lo rows into the same accumulator.
+template <int D, bool Q2 = false>
 struct Cfg {
     static constexpr int NCH = D / 64;                         // 64-dim (128-byte) chunks
     static constexpr uint32_t CHUNK = TR * 128;                // one chunk of a K or V tile
     static constexpr uint32_t KV_BYTES = NCH * CHUNK;          // one K (or V) tile
-    static constexpr uint32_t QCH = QROWS * 128;               // one chunk of Q' (32 rows)
+    static constexpr uint32_t Q_LO = QROWS * 128;              // offset of the lo rows in a chunk
+    static constexpr uint32_t QCH = (Q2 ? 2 : 1) * QROWS * 128;   // one chunk of Q' (32 or 64 rows)
     static constexpr uint32_t QBUF = NCH * QCH;
     static constexpr uint32_t OFF_Q = 0;                       // two Q' buffers
     static constexpr uint32_t OFF_RING = 2 * QBUF;             // the MMA reads 128 rows from a Q'
@@ -156,11 +160,11 @@ __device__ __forceinline__ void tcur_next(TileCur& c, const int* tpref, const De
     tcur_mark_last<TT>(c);
 }
 
-template <int D, int NH>
+template <int D, int NH, bool Q2>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const DecArgs A, const int q_rows) {
-    using C = Cfg<D>;
+    using C = Cfg<D, Q2>;
     constexpr int NCH = C::NCH, NK = C::NK, NV = C::NV;
     constexpr int NBX = 8 / NH;                 // 16-token boxes per MMA tile
     constexpr int TT = TR / NH;                 // tokens per MMA tile
@@ -245,12 +249,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(B_QFULL + qb), NCH * q_rows * 128);
+                    mbar_arrive_expect_tx(bar(B_QFULL + qb), (Q2 ? 2 : 1) * NCH * q_rows * 128);
                     q_last[qb] = c.run;
 #pragma unroll
-                    for (int ch = 0; ch < NCH; ++ch)
+                    for (int ch = 0; ch < NCH; ++ch) {
                         tma_load_3d(sbase + C::OFF_Q + qb * C::QBUF + ch * C::QCH, &tm_q, bar(B_QFULL + qb), ch * 64,
                                     c.hb * QB, c.b);
+                        // Q2: the lo terms sit B "sequences" further on in the same map
+                        if constexpr (Q2)
+                            tma_load_3d(sbase + C::OFF_Q + qb * C::QBUF + ch * C::QCH + C::Q_LO, &tm_q,
+                                        bar(B_QFULL + qb), ch * 64, c.hb * QB, c.b + A.B);
+                    }
                 }
                 const int slot = j % NS;
                 if (j >= (uint32_t)NS &&
@@ -319,6 +328,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const uint64_t a = smem_desc_sw128(qb + ch * C::QCH + kk * 32, 16, 1024);
                         const uint64_t b = smem_desc_sw128(kb + ch * C::CHUNK + kk * 32, 16, 1024);
                         tc_mma_f16_ss(tmem + C::COL_S, a, b, idesc_s, (ch | kk) != 0);
+                        if constexpr (Q2) {
+                            const uint64_t a_lo = smem_desc_sw128(qb + ch * C::QCH + C::Q_LO + kk * 32, 16, 1024);
+                            tc_mma_f16_ss(tmem + C::COL_S, a_lo, b, idesc_s, 1u);
+                        }
                     }
                 tc_commit(bar(B_SFULL));
                 tc_commit(bar(B_KEMPTY + slot));

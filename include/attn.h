@@ -53,6 +53,13 @@ typedef enum {
                                K and V scale buffers) */
 } attn_kv_dtype;
 
+/* Element type of decode queries and outputs (attn_decode_ex, attn_decode_tiered). */
+typedef enum {
+    ATTN_F16 = 0,           /* IEEE binary16 */
+    ATTN_F32 = 1            /* IEEE binary32 (attention.js: the int8 tier requires f32 Q;
+                               outputDtype f16 or f32 per variant) */
+} attn_dtype;
+
 /* Library version, e.g. "libattn 0.1.0 sm_103a". */
 const char* attn_version(void);
 
@@ -154,6 +161,35 @@ attn_status attn_decode_ring(const void* q, const void* k_ring, const void* v_ri
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_ex -- attn_decode with every cache layout and the query and
+ * output element types as arguments.
+ *
+ *  q, q_dtype      device [B, Hq, D] of ATTN_F16 or ATTN_F32.  f32 queries keep
+ *                    their precision: the tensor-core kernel multiplies two f16
+ *                    terms hi + lo (hi = f16(q), lo = f16(q - hi)) into one
+ *                    accumulator; the CUDA-core kernel reads them as f32.
+ *  ring_size       > 0 selects the ring layout of attn_decode_ring (kv_len is
+ *                    then the logical length, page_table must be NULL and max_kv
+ *                    is ignored); 0 selects attn_decode's contiguous or paged
+ *                    layout.
+ *  out, out_dtype  device [B, Hq, D] of ATTN_F16 (rounded to nearest even) or
+ *                    ATTN_F32.
+ *  The other arguments, the workspace (attn_decode_workspace_size with max_kv,
+ *  or ring_size for a ring) and the errors are attn_decode's.  With f16 q and
+ *  f16 out the result is attn_decode's bit for bit; f32 out holds the same
+ *  values before their rounding to f16.
+ */
+attn_status attn_decode_ex(const void* q, attn_dtype q_dtype,
+                           const void* k_cache, const void* v_cache,
+                           const int32_t* kv_len, const int32_t* page_table,
+                           int page_size, int max_pages_per_seq, int n_pages, int max_kv, int ring_size,
+                           const void* k_scales, const void* v_scales, attn_kv_dtype kv_dtype,
+                           int batch, int n_heads, int n_kv_heads, int head_dim,
+                           int window, float softcap, float scale, int split_keys,
+                           void* out, attn_dtype out_dtype, float* lse_out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_tiered -- decode over two tiers of one sequence's cache in one
  * call: a cold tier (the older tokens: contiguous or paged, f16 or int8 with
  * scales) and a hot tier (the newest tokens: an f16 ring).  (doppler
@@ -180,6 +216,8 @@ attn_status attn_decode_ring(const void* q, const void* k_ring, const void* v_ri
  *  Positions: cold token j at j, hot token i at cold_len + i; the query is the
  *  newest token, at cold_len + hot_len - 1.  window W > 0 keeps the keys whose
  *  position is within W of the query (it may end inside either tier); 0 = off.
+ *  q_dtype,    the element types of q and out, as in attn_decode_ex (the
+ *  out_dtype     int8 tier of the pages takes f32 q).
  *  The other arguments are those of attn_decode; out and lse_out receive one
  *  softmax over the kept keys of both tiers.  A sequence with no kept key gets
  *  a zero row and lse = -inf.
@@ -190,7 +228,7 @@ attn_status attn_decode_ring(const void* q, const void* k_ring, const void* v_ri
  */
 size_t attn_decode_tiered_workspace_size(int batch, int n_heads, int n_kv_heads, int head_dim,
                                          int cold_max_kv, int hot_ring, int split_keys);
-attn_status attn_decode_tiered(const void* q,
+attn_status attn_decode_tiered(const void* q, attn_dtype q_dtype,
                                const void* cold_k, const void* cold_v,
                                const void* cold_k_scales, const void* cold_v_scales,
                                attn_kv_dtype cold_dtype, const int32_t* cold_len,
@@ -200,7 +238,7 @@ attn_status attn_decode_tiered(const void* q,
                                const int32_t* hot_len, const int32_t* hot_start, int hot_ring,
                                int batch, int n_heads, int n_kv_heads, int head_dim,
                                int window, float softcap, float scale, int split_keys,
-                               void* out, float* lse_out,
+                               void* out, attn_dtype out_dtype, float* lse_out,
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*

@@ -127,7 +127,8 @@ def test_decode_ring_rejects_bad_arguments_on_host(lib, kw, status):
 
 
 def _decode_tiered(**kw):
-    args = dict(q=FAKE, cold_k=FAKE, cold_v=FAKE, cold_k_scales=None, cold_v_scales=None,
+    args = dict(q=FAKE, q_dtype=attn.ATTN_F16, out_dtype=attn.ATTN_F16, cold_k=FAKE, cold_v=FAKE,
+                cold_k_scales=None, cold_v_scales=None,
                 cold_dtype=attn.ATTN_KV_F16, cold_len=FAKE, cold_page_table=None, cold_page_size=0,
                 cold_max_pages_per_seq=0, cold_n_pages=0, cold_max_kv=128, hot_k=FAKE, hot_v=FAKE, hot_len=FAKE,
                 hot_start=FAKE, hot_ring=64, batch=1, n_heads=4, n_kv_heads=2, head_dim=64, window=0, softcap=0.0,
@@ -135,10 +136,10 @@ def _decode_tiered(**kw):
                 stream=0)
     args.update(kw)
     return attn.load().attn_decode_tiered(*[args[k] for k in (
-        "q", "cold_k", "cold_v", "cold_k_scales", "cold_v_scales", "cold_dtype", "cold_len", "cold_page_table",
-        "cold_page_size", "cold_max_pages_per_seq", "cold_n_pages", "cold_max_kv", "hot_k", "hot_v", "hot_len",
-        "hot_start", "hot_ring", "batch", "n_heads", "n_kv_heads", "head_dim", "window", "softcap", "scale",
-        "split_keys", "out", "lse_out", "workspace", "workspace_bytes", "stream")])
+        "q", "q_dtype", "cold_k", "cold_v", "cold_k_scales", "cold_v_scales", "cold_dtype", "cold_len",
+        "cold_page_table", "cold_page_size", "cold_max_pages_per_seq", "cold_n_pages", "cold_max_kv", "hot_k", "hot_v",
+        "hot_len", "hot_start", "hot_ring", "batch", "n_heads", "n_kv_heads", "head_dim", "window", "softcap", "scale",
+        "split_keys", "out", "out_dtype", "lse_out", "workspace", "workspace_bytes", "stream")])
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -153,6 +154,8 @@ def _decode_tiered(**kw):
     (dict(head_dim=80), attn.ATTN_EUNSUPPORTED),
     (dict(workspace_bytes=64), attn.ATTN_EINVAL),
     (dict(hot_v=FAKE + 4), attn.ATTN_EINVAL),                            # misaligned
+    (dict(q_dtype=2), attn.ATTN_EINVAL),
+    (dict(out_dtype=7), attn.ATTN_EINVAL),
 ])
 def test_decode_tiered_rejects_bad_arguments_on_host(lib, kw, status):
     assert _decode_tiered(**kw) == status
@@ -165,6 +168,34 @@ def test_tiered_workspace_is_both_plans(lib):
     t = attn.attn_decode_tiered_workspace_size(4, 32, 8, 128, 8192, 1024)
     assert t >= a + h and t < a + h + 256
     assert attn.attn_decode_tiered_workspace_size(4, 32, 8, 128, 8192, 1000) == 0    # ring % 16
+
+
+def _decode_ex(**kw):
+    args = dict(q=FAKE, q_dtype=attn.ATTN_F32, k_cache=FAKE, v_cache=FAKE, kv_len=FAKE, page_table=None,
+                page_size=0, max_pages_per_seq=0, n_pages=0, max_kv=128, ring_size=0, k_scales=None, v_scales=None,
+                kv_dtype=attn.ATTN_KV_F16, batch=1, n_heads=4, n_kv_heads=2, head_dim=64, window=0, softcap=0.0,
+                scale=0.125, split_keys=0, out=FAKE, out_dtype=attn.ATTN_F32, lse_out=None, workspace=FAKE,
+                workspace_bytes=1 << 30, stream=0)
+    args.update(kw)
+    return attn.load().attn_decode_ex(*[args[k] for k in (
+        "q", "q_dtype", "k_cache", "v_cache", "kv_len", "page_table", "page_size", "max_pages_per_seq", "n_pages",
+        "max_kv", "ring_size", "k_scales", "v_scales", "kv_dtype", "batch", "n_heads", "n_kv_heads", "head_dim",
+        "window", "softcap", "scale", "split_keys", "out", "out_dtype", "lse_out", "workspace", "workspace_bytes",
+        "stream")])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q_dtype=3), attn.ATTN_EINVAL),
+    (dict(out_dtype=-1), attn.ATTN_EINVAL),
+    (dict(ring_size=20), attn.ATTN_EUNSUPPORTED),
+    (dict(ring_size=32, page_table=FAKE, page_size=16, max_pages_per_seq=2, n_pages=4), attn.ATTN_EINVAL),
+    (dict(q=FAKE + 8), attn.ATTN_EINVAL),                                 # misaligned
+    (dict(head_dim=32), attn.ATTN_EUNSUPPORTED),
+    (dict(workspace_bytes=16), attn.ATTN_EINVAL),
+])
+def test_decode_ex_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _decode_ex(**kw) == status
+    assert attn.attn_last_error()
 
 
 def _prefill(**kw):

@@ -94,7 +94,7 @@ def test_tiered_rejects_bad_hot_ring():
     ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
     for bad in (0, 8, 40):
         with pytest.raises(attn.AttnError) as e:
-            attn.attn_decode_tiered(c.q, c.k, c.v, None, None, attn.ATTN_KV_F16, c.kv_len, None, 0, 0, 0, c.cap,
-                                    c.hot_k, c.hot_v, c.hot_len, c.hot_start, bad, 1, 4, 2, 64, 0, 0.0, 0.125, 0,
-                                    out, None, ws, ws.numel())
+            attn.attn_decode_tiered(c.q, attn.ATTN_F16, c.k, c.v, None, None, attn.ATTN_KV_F16, c.kv_len, None, 0, 0,
+                                    0, c.cap, c.hot_k, c.hot_v, c.hot_len, c.hot_start, bad, 1, 4, 2, 64, 0, 0.0,
+                                    0.125, 0, out, attn.ATTN_F16, None, ws, ws.numel())
         assert e.value.status == attn.ATTN_EUNSUPPORTED
