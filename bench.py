@@ -11,7 +11,8 @@ masks, online softmax, PV, split combine, tensor-core prefill tiles):
   int8_long_decode     B=16, 32q/8kv heads, D=128, kv_len 32768, int8 K/V + f16 scales
   chunked_prefill_paged  B=8, 512-token chunks on 512..7680 cached tokens, 16-token pages
   ring_window_decode   B=32, 32q/8kv heads, D=128, 4096-slot ring, logical kv_len 4K..64K
-  tiered_int8_decode   B=32, 32q/8kv heads, D=128, int8 paged cold tier 2K..16K + f16 1024-slot hot ring
+  tiered_int8_decode   B=32, 32q/8kv heads, D=128, int8 paged cold tier 2K..16K + f16 1024-slot hot ring, f32 q
+  paged_decode_f32io   paged_gqa_decode's shape and lengths with f32 queries and f32 outputs
 
 The headline metric is the vision workload's TFLOP/s (algorithmic FLOPs
 4*S^2*D*H over the call's CUDA-event time); decode workloads report KV GB/s.
@@ -59,7 +60,7 @@ NCU_TRAFFIC = {
 }
 METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
 WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode",
-                  "chunked_prefill_paged", "ring_window_decode", "tiered_int8_decode"]
+                  "chunked_prefill_paged", "ring_window_decode", "tiered_int8_decode", "paged_decode_f32io"]
 L2_FLUSH_BYTES = 256 << 20
 HOST_SLACK_CYCLES = 200_000   # about 0.1 ms of device time before each timed call
 
@@ -109,7 +110,7 @@ def chunk_flops(case):
     return 4.0 * case.head_dim * pairs * case.n_heads
 
 
-def decode_bytes(case):
+def decode_bytes(case, out_bytes=2):
     """KV bytes a decode call must read once, plus q, out, kv_len and page table."""
     esz = 1 if case.int8 else 2
     per_tok = case.n_kv_heads * case.head_dim * esz * 2 + (case.n_kv_heads * 2 * 2 if case.int8 else 0)
@@ -123,11 +124,11 @@ def decode_bytes(case):
         kv += Le * per_tok
         if case.paged:
             pages += (L + case.page_size - 1) // case.page_size
-    qo = 2 * case.batch * case.n_heads * case.head_dim * 2
+    qo = case.batch * case.n_heads * case.head_dim * (case.q.element_size() + out_bytes)
     return kv + qo + case.batch * 4 + pages * 4
 
 
-def tiered_bytes(case):
+def tiered_bytes(case, out_bytes=2):
     """KV bytes a tiered decode call must read once: the kept cold tokens (codes
     and scales for int8), the kept hot tokens (f16), plus q, out, the length and
     start arrays and the cold page table."""
@@ -147,7 +148,7 @@ def tiered_bytes(case):
         kv += ck * cold_tok + hk * hot_tok
         if case.paged:
             pages += (Lc + case.page_size - 1) // case.page_size
-    qo = 2 * case.batch * case.n_heads * case.head_dim * 2
+    qo = case.batch * case.n_heads * case.head_dim * (case.q.element_size() + out_bytes)
     return kv + qo + 3 * case.batch * 4 + pages * 4
 
 
@@ -165,10 +166,12 @@ def workload_config(case):
         return {"global_batch": case.batch, "n_heads": case.n_heads, "n_kv_heads": case.n_kv_heads,
                 "head_dim": case.head_dim, "cold_len_min": min(case.lens), "cold_len_max": max(case.lens),
                 "cold_kv_dtype": "int8" if case.int8 else "f16", "cold_page_size": case.page_size,
-                "hot_ring": case.hot_ring, "hot_len_min": min(case.hot_lens), "hot_len_max": max(case.hot_lens)}
+                "hot_ring": case.hot_ring, "hot_len_min": min(case.hot_lens), "hot_len_max": max(case.hot_lens),
+                "q_dtype": "f32" if case.q.element_size() == 4 else "f16"}
     return {"global_batch": case.batch, "n_heads": case.n_heads, "n_kv_heads": case.n_kv_heads,
             "head_dim": case.head_dim, "kv_len_min": min(case.lens), "kv_len_max": max(case.lens),
             "kv_dtype": "int8" if case.int8 else "f16", "page_size": case.page_size,
+            "q_dtype": "f32" if case.q.element_size() == 4 else "f16",
             **({"ring": case.ring} if getattr(case, "ring", 0) else {})}
 
 
@@ -371,16 +374,20 @@ def main(argv=None):
         if si.WORKLOADS[n]["kind"] == "decode":
             ws = torch.empty(attn.attn_decode_workspace_size(c.batch, c.n_heads, c.n_kv_heads, c.head_dim,
                                                              c.cap), dtype=torch.uint8, device=dev)
-            out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float16, device=dev)
+            o32 = bool(si.WORKLOADS[n].get("out_f32"))
+            out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float32 if o32 else torch.float16,
+                              device=dev)
             runs[n] = (lambda c=c, ws=ws, out=out: attn.decode(c, out=out, workspace=ws))
-            work[n] = ("GB/s", decode_bytes(c), "hbm", 2)
+            # f32 queries on the tensor-core kernel add the hi/lo split launch
+            extra = 1 if (c.q.dtype == torch.float32 and not c.int8 and c.head_dim != 256) else 0
+            work[n] = ("GB/s", decode_bytes(c, 4 if o32 else 2), "hbm", 2 + extra)
         elif si.WORKLOADS[n]["kind"] == "tiered":
             ws = torch.empty(attn.attn_decode_tiered_workspace_size(c.batch, c.n_heads, c.n_kv_heads, c.head_dim,
                                                                     c.cap, c.hot_ring), dtype=torch.uint8,
                              device=dev)
             out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float16, device=dev)
             runs[n] = (lambda c=c, ws=ws, out=out: attn.decode_tiered(c, out=out, workspace=ws))
-            work[n] = ("GB/s", tiered_bytes(c), "hbm", 3)
+            work[n] = ("GB/s", tiered_bytes(c), "hbm", 3 + (1 if c.q.dtype == torch.float32 else 0))
         elif si.WORKLOADS[n]["kind"] == "chunked":
             out = torch.empty_like(c.q)
             runs[n] = (lambda c=c, out=out: attn.prefill_paged(c, out=out))

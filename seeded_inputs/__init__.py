@@ -498,9 +498,14 @@ WORKLOADS = {
     # tiered decode, the int8 tier of the pages: 32 sequences, an int8 cold tier of
     # 2K..16K tokens on 16-token pages plus an f16 hot ring of 1024 slots holding
     # the newest 256..1024 tokens
+    # (f32 queries, as the pages' int8 tier requires)
     "tiered_int8_decode": dict(kind="tiered", seed=8, batch=32, n_heads=32, n_kv_heads=8, head_dim=128,
                                cold_lens=(2048, 16384), hot_lens=(256, 1024), hot_ring=1024, int8=True,
-                               page_size=16, window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
+                               page_size=16, window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0), q_f32=True),
+    # the paged GQA decode with f32 queries and f32 outputs
+    "paged_decode_f32io": dict(kind="decode", seed=9, batch=32, n_heads=32, n_kv_heads=8, head_dim=128,
+                               lens=(512, 8192), int8=False, page_size=16, n_pages=None, window=0, softcap=0.0,
+                               scale=1.0 / math.sqrt(128.0), q_f32=True, out_f32=True),
     "chunked_prefill_paged": dict(kind="chunked", seed=6, batch=8, n_heads=32, n_kv_heads=8,
                                   head_dim=128, q_lens=[512] * 8, ctx_lens=(512, 7680), page_size=16,
                                   window=0, softcap=0.0, scale=1.0 / math.sqrt(128.0)),
@@ -523,6 +528,7 @@ def make_workload(name: str, device: str = "cpu"):
     w = dict(WORKLOADS[name])
     kind = w.pop("kind")
     seed = w.pop("seed")
+    w.pop("out_f32", None)   # an output type: the caller allocates out
     if kind == "decode":
         b, hq, hkv, d, lens = (w.pop("batch"), w.pop("n_heads"), w.pop("n_kv_heads"),
                                w.pop("head_dim"), w.pop("lens"))

@@ -30,11 +30,12 @@ def _sample_rows(n_outer, n_heads, k, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["tiny_decode", "paged_gqa_decode", "int8_long_decode", "ring_window_decode"])
+@pytest.mark.parametrize("name", ["tiny_decode", "paged_gqa_decode", "int8_long_decode", "ring_window_decode",
+                                  "paged_decode_f32io"])
 def test_decode_workload(name):
     g = si.make_workload(name, device="cuda")
     lse = torch.empty((g.batch, g.n_heads), dtype=torch.float32, device="cuda")
-    out = attn.decode(g, lse_out=lse)
+    out = attn.decode(g, lse_out=lse, out_f32=bool(si.WORKLOADS[name].get("out_f32")))
     torch.cuda.synchronize()
     cpu = g.to("cpu")
     if name == "tiny_decode":
