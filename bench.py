@@ -53,10 +53,11 @@ HEADLINE = "vision_2304"
 NCU_TRAFFIC = {
     "vision_2304": 14.24e6,
     "swa_softcap_prefill": 33.62e6,
-    "paged_gqa_decode": 583.4e6,
-    "int8_long_decode": (136.53e6 + 8.13e6) * 8,
+    "paged_gqa_decode": 583.3e6,
+    "int8_long_decode": (136.54e6 + 8.53e6) * 8,
     "chunked_prefill_paged": 237.95e6,
     "ring_window_decode": 543.1e6,
+    "paged_decode_f32io": 593.2e6,
 }
 METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
 WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode",
