@@ -20,8 +20,9 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "attn_oracle.c")
-_OUT_DIR = os.path.join(_HERE, "_build")
+# the mutation tests point these at a deliberately broken copy of the source
+_SRC = os.environ.get("ATTN_ORACLE_SRC") or os.path.join(_HERE, "attn_oracle.c")
+_OUT_DIR = os.environ.get("ATTN_ORACLE_BUILD") or os.path.join(_HERE, "_build")
 _LIB = os.path.join(_OUT_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
