@@ -114,6 +114,10 @@ struct PrefillCfg {
 // 3 of 8 and 41.7 at 4 of 8).
 constexpr int kPolyPerEight = 0;
 
+// A row whose exponentials against the running max sum to at most this (2 to the
+// lazy-rescale threshold) keeps them: no tile max needed.
+constexpr float kFastSumLimit = 256.0f;
+
 // 2^x on the FMA/ALU pipes: n = round(x) (added to the float 1.5*2^23 so that
 // the rounding lands n in the low mantissa bits), f = x - n in [-1/2, 1/2],
 // 2^f by a cubic minimax fit (relative error 7.5e-5, below the f16 rounding
@@ -565,51 +569,76 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (!keep) t[i] = -INFINITY;
                 }
             }
-            float mx = row_max(t);
-            if constexpr (SPLIT) {
-                float other;
-                if (!exchange(mx, 2 * (j & 1), j, other)) { ok = false; break; }
-                mx = fmaxf(mx, other);
-            }
-            const float m_tile = MODE == kModeRaw ? mx * scale_log2 : mx;
-            const bool need = m_tile > m_used + kRescaleThreshold || (m_used == -INFINITY && m_tile > -INFINITY);
-            // the warp rescales O (below, once t[] is no longer live) if any of its rows moved its max
-            const bool rescale = __any_sync(0xffffffffu, need) && j > 0;
-            float alpha_o = 1.f;
-            if (need) {
-                const float m_new = fmaxf(m_tile, m_used);
-                const float alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
-                alpha_o = alpha;
-                l_sum *= alpha;
-                m_used = m_new;
-            }
-            const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
             // P buffer j % NBUF is free once PV_{j-NBUF} has retired
-            if (j >= NBUF && !mbar_wait(bar(B_PVDONE + (j % NBUF)), ((j - NBUF) / NBUF) & 1, abort_flag, args.err, kErrTimeoutMma)) { ok = false; break; }
-            // pairs of elements in packed f32x2 arithmetic: x = t*scale - m (or t - m), p = 2^x
-            float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                            make_float2(0.f, 0.f)};   // independent partial sums (short dependency chains)
+            auto p_free = [&]() -> bool {
+                return j < NBUF || mbar_wait(bar(B_PVDONE + (j % NBUF)), ((j - NBUF) / NBUF) & 1, abort_flag,
+                                             args.err, kErrTimeoutMma);
+            };
             const float2 sl2 = make_float2(scale_log2, scale_log2);
-            const float2 nm2 = make_float2(-m_off, -m_off);
             const uint32_t p_addr = lane_base + C::COL_P + (j % NBUF) * C::P_COLS + ch * (CW / 2);
-            // 32 elements at a time, each chunk stored to TMEM as soon as it is packed
+            // p = 2^(t*scale - m_off) (or 2^(t - m_off)) in packed f32x2 arithmetic, packed to
+            // f16 and stored to TMEM 32 elements at a time; returns the row's sum of p
+            auto exps = [&](float m_off) -> float {
+                float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};   // independent partial sums (short dependency chains)
+                const float2 nm2 = make_float2(-m_off, -m_off);
 #pragma unroll
-            for (int c = 0; c < CW / 32; ++c) {
-                uint32_t packed[16];
+                for (int c = 0; c < CW / 32; ++c) {
+                    uint32_t packed[16];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float2 ti = make_float2(t[c * 32 + i], t[c * 32 + i + 1]);
-                    const float2 x = MODE == kModeRaw ? ffma2(ti, sl2, nm2) : fadd2(ti, nm2);
-                    const bool poly = (i & 7) < kPolyPerEight;
-                    const float2 p = poly ? ex2_poly2(x) : make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    const __half2 hp = __floats2half2_rn(p.x, p.y);
-                    ls[(i / 2) & 3] = fadd2(ls[(i / 2) & 3], p);
-                    packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 ti = make_float2(t[c * 32 + i], t[c * 32 + i + 1]);
+                        const float2 x = MODE == kModeRaw ? ffma2(ti, sl2, nm2) : fadd2(ti, nm2);
+                        const bool poly = (i & 7) < kPolyPerEight;
+                        const float2 p = poly ? ex2_poly2(x) : make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        const __half2 hp = __floats2half2_rn(p.x, p.y);
+                        ls[(i / 2) & 3] = fadd2(ls[(i / 2) & 3], p);
+                        packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+                    }
+                    tc_st_32x32b_x16(p_addr + c * 16, packed);
                 }
-                tc_st_32x32b_x16(p_addr + c * 16, packed);
+                const float2 lsum2 = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
+                return lsum2.x + lsum2.y;
+            };
+            // Optimistic pass (whole rows only): exponentials against the running max,
+            // without the tile's max.  A row whose p sum to at most 2^8 has every p <= 2^8,
+            // the bound the lazy rescale keeps; a warp with any other row (or a NaN) redoes
+            // the tile below with the tile's max, overwriting P.
+            bool fast = false;
+            if constexpr (!SPLIT) {
+                if (__all_sync(0xffffffffu, m_used != -INFINITY)) {
+                    if (!p_free()) { ok = false; break; }
+                    const float lsum = exps(m_used);
+                    if (!__any_sync(0xffffffffu, !(lsum <= kFastSumLimit))) {
+                        l_sum += lsum;
+                        fast = true;
+                    }
+                }
             }
-            const float2 lsum2 = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
-            l_sum += lsum2.x + lsum2.y;
+            bool rescale = false;
+            float alpha_o = 1.f;
+            if (!fast) {
+                float mx = row_max(t);
+                if constexpr (SPLIT) {
+                    float other;
+                    if (!exchange(mx, 2 * (j & 1), j, other)) { ok = false; break; }
+                    mx = fmaxf(mx, other);
+                }
+                const float m_tile = MODE == kModeRaw ? mx * scale_log2 : mx;
+                const bool need = m_tile > m_used + kRescaleThreshold || (m_used == -INFINITY && m_tile > -INFINITY);
+                // the warp rescales O (below, once t[] is no longer live) if any of its rows moved its max
+                rescale = __any_sync(0xffffffffu, need) && j > 0;
+                if (need) {
+                    const float m_new = fmaxf(m_tile, m_used);
+                    const float alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
+                    alpha_o = alpha;
+                    l_sum *= alpha;
+                    m_used = m_new;
+                }
+                const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
+                if (!p_free()) { ok = false; break; }
+                l_sum += exps(m_off);
+            }
             if (rescale) {
                 // O must not be in flight while it is rescaled (PV_j waits for p_full below)
                 if (NBUF > 1 &&
