@@ -600,12 +600,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const float2 lsum2 = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
                 return lsum2.x + lsum2.y;
             };
-            // Optimistic pass (whole rows only): exponentials against the running max,
+            // Optimistic pass (D=128, whole rows): exponentials against the running max,
             // without the tile's max.  A row whose p sum to at most 2^8 has every p <= 2^8,
             // the bound the lazy rescale keeps; a warp with any other row (or a NaN) redoes
-            // the tile below with the tile's max, overwriting P.
+            // the tile below with the tile's max, overwriting P.  (Measured slower for
+            // D=64, whose 128-key tiles keep the max computation off the critical path.)
             bool fast = false;
-            if constexpr (!SPLIT) {
+            if constexpr (!SPLIT && D == 128) {
                 if (__all_sync(0xffffffffu, m_used != -INFINITY)) {
                     if (!p_free()) { ok = false; break; }
                     const float lsum = exps(m_used);
