@@ -18,9 +18,10 @@
  *   o_i = sum_j softmax_j(s) v_j[g] over the kept keys j, in fp32 with f16 I/O.
  * Sources: doppler src/gpu/kernels/attention.js (createAttentionUniformBuffer:
  * numHeads, numKVHeads, headDim, kvLen, seqLen, scale, causal, attnSoftcap
- * "0 = disabled", slidingWindow "0 = disabled", pageSize, kvLayout
- * contiguous/paged; executeAttention: the per-call kvLen buffer and page
- * table), doppler src/inference/pipelines/text/attention/run.js
+ * and slidingWindow (0 turns either off), pageSize, kvLayout
+ * contiguous/ring/paged; executeAttention: the per-call kvLen buffer and page
+ * table; executeAttentionTiered / executeAttentionTieredQuant: the hot and
+ * cold tiers), doppler src/inference/pipelines/text/attention/run.js
  * (runLayerAttentionGPU: the decode query sits at position kvLen-1, the
  * sliding-window clamp, scale = 1/sqrt(query_pre_attn_scalar)), and rullama
  * src/backend/dispatch/attention.rs (vision_attention_chained: bidirectional
@@ -56,7 +57,7 @@ typedef enum {
 /* Element type of decode queries and outputs (attn_decode_ex, attn_decode_tiered). */
 typedef enum {
     ATTN_F16 = 0,           /* IEEE binary16 */
-    ATTN_F32 = 1            /* IEEE binary32 (attention.js: the int8 tier requires f32 Q;
+    ATTN_F32 = 1            /* IEEE binary32 (attention.js: the int8 tier takes f32 Q only;
                                outputDtype f16 or f32 per variant) */
 } attn_dtype;
 

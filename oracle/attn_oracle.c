@@ -123,7 +123,7 @@ static void oracle_attend(const double* q, const double* K, const double* V,
 }
 
 /* One query element: q is f16 bits, or binary32 values when q_f32 (the f32-Q
- * variant: attention.js executeAttentionTieredQuant requires f32 Q; a float
+ * variant: attention.js executeAttentionTieredQuant takes f32 Q only; a float
  * widens to double exactly). */
 static double oracle_q_value(const void* q, int q_f32, long idx)
 {
