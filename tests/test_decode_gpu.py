@@ -108,6 +108,18 @@ def test_split_count_does_not_change_the_result(split_keys):
     assert np.abs(got - base).max() <= 2e-3
 
 
+@pytest.mark.parametrize("B", [2048, 2049, 4096])
+def test_decode_largest_batches(B):
+    # 2048 sequences is the tensor-core kernel's limit (its prefixes live in shared
+    # memory); 2049 falls back to the CUDA-core kernel; 4096 is the library's limit
+    lens = [(7 * b) % 61 for b in range(B)]   # 0 .. 60 keys, some empty
+    case = si.make_decode_case(B, 8, 2, 64, lens, seed=B, page_size=16)
+    ref, ref_lse = oracle.decode(case)
+    got, lse = _run(case)
+    assert_close(got.reshape(ref.shape), ref, what="batch %d" % B)
+    assert_lse_close(lse.reshape(-1), ref_lse, what="batch %d" % B)
+
+
 def test_zero_length_sequence():
     case = si.make_decode_case(3, 4, 2, 64, [0, 20, 0], seed=81, cap=32)
     got, lse = _run(case)
