@@ -28,6 +28,30 @@ def test_workload_work_figures():
     assert bench.decode_bytes(tiny) == 128 * 2 * 64 * 2 * 2 + 2 * 4 * 64 * 2 + 4
 
 
+def test_chunk_ring_tiered_and_f32_work_figures():
+    # chunked prefill: a chunk of n queries at the end of L keys keeps pos + 1 keys
+    # for query pos = L - n + i (none below position 0)
+    class Ch:
+        q_lens, kv_lens, window, head_dim, n_heads = [3, 2], [5, 1], 0, 8, 2
+    pairs = (3 + 4 + 5) + (1)   # sequence 0: positions 2,3,4; sequence 1: position 0 (and -1)
+    assert bench.chunk_flops(Ch) == 4 * 8 * pairs * 2
+    # ring: a 16-slot ring keeps min(L, 16) tokens whatever the logical length
+    c = si.make_decode_case(2, 4, 2, 16, [40, 7], seed=1, ring=16)
+    per_tok = 2 * 16 * 2 * 2
+    assert bench.decode_bytes(c) == (16 + 7) * per_tok + 2 * 4 * 16 * 2 + 2 * 4 * 16 * 2 + 2 * 4
+    # f32 queries and outputs: 4 bytes each instead of 2
+    c32 = si.make_decode_case(2, 4, 2, 16, [40, 7], seed=1, ring=16, q_f32=True)
+    assert bench.decode_bytes(c32, 4) == (16 + 7) * per_tok + 2 * 4 * 16 * 4 * 2 + 2 * 4
+    # tiered: kept cold tokens (int8 codes + 2 f16 scales per kv head) and kept hot ring tokens
+    t = si.make_tiered_case(2, 4, 2, 16, [10, 3], [20, 5], 16, seed=2, int8=True, window=12)
+    cold_tok = 2 * 16 * 2 + 2 * 2 * 2
+    hot_tok = 2 * 16 * 2 * 2
+    # window 12: sequence 0 keeps 12 hot tokens (of the 16 the ring holds) and no cold
+    # one; sequence 1 keeps its 5 hot tokens and min(3, 12 - 5) = 3 cold ones
+    kv = (0 * cold_tok + 12 * hot_tok) + (3 * cold_tok + 5 * hot_tok)
+    assert bench.tiered_bytes(t) == kv + 2 * 4 * 16 * (2 + 2) + 3 * 2 * 4
+
+
 def test_clock_summary_flags_throttle_reasons():
     lines = ["0, 1900, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Active",
              "0, 1950, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
