@@ -21,7 +21,7 @@ __all__ = [
     "attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
     "attn_decode_ring", "attn_decode_ex", "attn_decode_tiered", "attn_decode_tiered_workspace_size",
     "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate", "attn_device_status",
-    "decode", "decode_tiered", "prefill", "prefill_paged",
+    "attn_testing_set_waits", "decode", "decode_tiered", "prefill", "prefill_paged",
 ]
 
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_EBOUNDS, ATTN_ETIMEOUT = range(6)
@@ -38,7 +38,7 @@ _lib = None
 exported_symbols = ("attn_version", "attn_last_error", "attn_decode_workspace_size", "attn_decode",
                     "attn_decode_ring", "attn_decode_ex", "attn_decode_tiered", "attn_decode_tiered_workspace_size",
                     "attn_decode_noalloc", "attn_prefill", "attn_prefill_paged", "attn_decode_validate",
-                    "attn_device_status")
+                    "attn_device_status", "attn_testing_set_waits")
 
 
 class AttnLibraryMissing(RuntimeError):
@@ -95,6 +95,8 @@ def load():
     lib.attn_decode_validate.restype = I
     lib.attn_device_status.argtypes = [P]
     lib.attn_device_status.restype = I
+    lib.attn_testing_set_waits.argtypes = [ctypes.c_ulonglong, I]
+    lib.attn_testing_set_waits.restype = I
     _lib = lib
     return lib
 
@@ -251,6 +253,11 @@ def attn_device_status(stream=None) -> int:
 
 
 # ---------------------------------------------------------------- conveniences
+def attn_testing_set_waits(wait_limit_ns: int, stall_first_tile: int) -> int:
+    """Testing hook: pipeline-wait time limit (0 = the default) and the first-tile stall."""
+    return load().attn_testing_set_waits(int(wait_limit_ns), int(stall_first_tile))
+
+
 def decode(case, out=None, lse_out=None, workspace=None, split_keys: int = 0, max_kv: Optional[int] = None,
            stream=None, out_f32=False):
     """attn_decode on a DecodeCase-like object (tensors already on the GPU);

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -81,6 +82,24 @@ attn_status set_error(attn_status st, const char* fmt, ...) {
     vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
     va_end(ap);
     return st;
+}
+
+bool trace_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("ATTN_TRACE");
+        return e != nullptr && e[0] != '\0' && std::strcmp(e, "0") != 0;
+    }();
+    return on;
+}
+
+void trace(const char* fmt, ...) {
+    if (!trace_enabled()) return;
+    char line[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(line, sizeof(line), fmt, ap);
+    va_end(ap);
+    std::fprintf(stderr, "[libattn] %s\n", line);
 }
 
 int* device_error_word() {
@@ -524,6 +543,15 @@ attn_status attn_decode_validate(const int32_t* kv_len, const int32_t* page_tabl
     if (bad_seq) *bad_seq = seq;
     return set_error((attn_status)code, "attn_decode_validate: sequence %d has %s", seq,
                      code == ATTN_EINVAL ? "kv_len <= 0" : "kv_len above capacity or a page id out of range");
+}
+
+attn_status attn_testing_set_waits(unsigned long long wait_limit_ns, int stall_first_tile) {
+    if (stall_first_tile != 0 && stall_first_tile != 1)
+        return set_error(ATTN_EINVAL, "attn_testing_set_waits: stall_first_tile must be 0 or 1");
+    const unsigned long long limit = wait_limit_ns ? wait_limit_ns : 4000000000ull;
+    attn_status st = set_test_controls_prefill(limit, stall_first_tile);
+    if (st == ATTN_OK) st = set_test_controls_decode(limit, stall_first_tile);
+    return st;
 }
 
 attn_status attn_device_status(void* stream) {

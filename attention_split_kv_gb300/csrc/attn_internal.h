@@ -24,6 +24,12 @@ enum : int {
 // Records a message for attn_last_error() (thread-local) and returns `st`.
 attn_status set_error(attn_status st, const char* fmt, ...);
 
+// Launch-configuration trace: with ATTN_TRACE set to anything but "" or "0"
+// in the environment, every launch is described on stderr (one line each:
+// kernel, grid, block, shared memory, split plan).  Off by default.
+bool trace_enabled();
+void trace(const char* fmt, ...);
+
 // Device error word (a file-scope __device__ int), as a device pointer.
 int* device_error_word();
 
@@ -109,6 +115,11 @@ bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys,
 attn_status launch_decode(const DecodeLaunch& L, const DecodePlan& plan);
 attn_status launch_decode_tiered(const DecodeLaunch& cold, const DecodePlan& cold_plan, const DecodeLaunch& hot,
                                  const DecodePlan& hot_plan);
+
+// Test controls of the prefill and decode translation units: the time limit
+// of pipeline waits (ns) and the first-tile stall (see ptx.cuh).
+attn_status set_test_controls_prefill(unsigned long long wait_limit_ns, int stall);
+attn_status set_test_controls_decode(unsigned long long wait_limit_ns, int stall);
 
 constexpr int kDecodeMaxBatch = 4096;
 constexpr int kDecodeMaxFix = 256;    // most CTAs the balanced decode kernel launches (>= SMs)

@@ -322,9 +322,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const uint32_t sbb = (box_sc + 127) / 128 * 128;          // scale boxes start 128-byte aligned
     bool ok = true;
 
+    // testing hook: issue nothing, so that the consumers' wait for the first
+    // tile runs out (the failure path, without a fault)
+    const bool stall = stall_first_tile();
     // Issue tiles until `target` (a consumption count) is covered.  Whole warp 0.
     auto produce_until = [&](uint32_t target) {
-        while (ok && issued <= target && p_it < total) {
+        while (ok && !stall && issued <= target && p_it < total) {
             const int t0 = p_item.ks + p_i * T;
             const int slot = issued % NSLOT;
             const int g0 = (p_item.hb * NW) / A.HG;
@@ -646,10 +649,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
     if (warp == 0 && !ok && lane == 0) {
         // let copies in flight land before shared memory is released
-        volatile int never = 0;
         const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
         for (uint32_t x = first; x < issued; ++x)
-            mbar_wait(full_bar(x % NSLOT), (x / NSLOT) & 1, &never, A.err, kErrTimeoutLoad);
+            mbar_wait_drain(full_bar(x % NSLOT), (x / NSLOT) & 1, A.err, kErrTimeoutLoad);
     }
 }
 
@@ -929,6 +931,9 @@ attn_status launch_combine(const DecodeLaunch& L, const DecodePlan& plan, const 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (trace_enabled())
+        trace("decode_combine_kernel<D=%d,tiers=%d,out=%s> grid=%u block=128 (one warp per (sequence, head); "
+              "programmatic dependent launch)", D, NT, L.out_f32 ? "f32" : "f16", cfg.gridDim.x);
     cudaError_t e = L.out_f32
         ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, NT, float>, T, static_cast<float*>(L.out), L.lse, L.B,
                              L.Hq, L.Hq / L.Hkv, plan.GH, plan.HG, plan.n_hb)
@@ -968,6 +973,7 @@ attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, Spli
         __half* hl = reinterpret_cast<__half*>(static_cast<uint8_t*>(L.workspace) + plan.off_qsplit);
         const long n = (long)L.B * L.Hq * D;
         const int blocks = (int)((n + 255) / 256 < 4 * sm_count() ? (n + 255) / 256 : 4 * sm_count());
+        if (trace_enabled()) trace("q_split_kernel grid=%d block=256 (f32 q -> f16 hi + lo)", blocks);
         q_split_kernel<<<blocks, 256, 0, L.stream>>>(static_cast<const float*>(L.q), hl, n);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(ATTN_ECUDA, "q split launch failed: %s", cudaGetErrorString(e));
@@ -1009,6 +1015,13 @@ attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, Spli
     const DecArgs a = make_dec_args(L, plan, 16);
     // balanced: every CTA takes an equal share of the tiles (see decode_tc.cuh)
     const int grid = sm_count() < plan.n_fix ? sm_count() : plan.n_fix;
+    if (trace_enabled())
+        trace("decode_tc_kernel<D=%d,NH=%d,f32q=%d> grid=%d block=%d smem=%u B=%d Hq=%d Hkv=%d layout=%s "
+              "tier=%d split=%d head_blocks=%d units=%d max_items=%ld tile_tokens=%d ring_slots=%d+%d "
+              "(tiles balanced over the CTAs)",
+              D, NH, (int)Q2, grid, tcdec::kThreads, C::SMEM_ALLOC, L.B, L.Hq, L.Hkv,
+              paged ? "paged" : L.ring > 0 ? "ring" : "contiguous", L.tier, plan.split, plan.n_hb, a.U,
+              plan.max_items, tcdec::TR / NH, C::NK, C::NV);
     tcdec::decode_tc_kernel<D, NH, Q2><<<grid, tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a, q_rows);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode tc launch failed: %s", cudaGetErrorString(e));
@@ -1082,6 +1095,13 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan, Split
         attr_set[dev] = true;
     }
     const DecArgs a = make_dec_args(L, plan, R);
+    if (trace_enabled())
+        trace("decode_split_kernel<D=%d,int8=%d,GH=%d> grid=%d block=%d smem=%d B=%d Hq=%d Hkv=%d layout=%s tier=%d "
+              "split=%d head_blocks=%d box_heads=%d box_rows=%d max_items=%ld ring_slots=%d "
+              "(items round-robin over the CTAs)",
+              D, (int)I8, GH, decode_grid(plan), kDecThreads, C::SMEM_ALLOC, L.B, L.Hq, L.Hkv,
+              paged ? "paged" : L.ring > 0 ? "ring" : "contiguous", L.tier, plan.split, plan.n_hb, plan.nh_box, R,
+              plan.max_items, C::NSLOT);
     decode_split_kernel<D, I8, GH><<<decode_grid(plan), kDecThreads, C::SMEM_ALLOC, L.stream>>>(tk, tv, tks, tvs, a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode split launch failed: %s", cudaGetErrorString(e));
@@ -1186,6 +1206,14 @@ attn_status launch_decode_tiered(const DecodeLaunch& cold, const DecodePlan& col
     T.t[0] = comb_tier(sc);
     T.t[1] = comb_tier(sh);
     return launch_combine_d<2>(cold, cold_plan, T);
+}
+
+// Sets this translation unit's test controls (see ptx.cuh).
+attn_status set_test_controls_decode(unsigned long long wait_limit_ns, int stall) {
+    if (cudaMemcpyToSymbol(g_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_stall_first_tile, &stall, sizeof(stall)) != cudaSuccess)
+        return set_error(ATTN_ECUDA, "test controls (decode): %s", cudaGetErrorString(cudaGetLastError()));
+    return ATTN_OK;
 }
 
 }  // namespace attn

@@ -291,12 +291,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             if (!ok) {
                 // let copies in flight land before shared memory is released
-                volatile int never = 0;
                 const uint32_t first = j > (uint32_t)NS ? j - NS : 0;
                 for (uint32_t x = first; x < j; ++x)
-                    mbar_wait(bar(b_full + (x % NS)), (x / NS) & 1, &never, A.err, kErrTimeoutLoad);
+                    mbar_wait_drain(bar(b_full + (x % NS)), (x / NS) & 1, A.err, kErrTimeoutLoad);
                 for (int qb = 0; qb < 2; ++qb)
-                    if (q_last[qb] >= 0) mbar_wait(bar(B_QFULL + qb), (q_last[qb] >> 1) & 1, &never, A.err, kErrTimeoutLoad);
+                    if (q_last[qb] >= 0) mbar_wait_drain(bar(B_QFULL + qb), (q_last[qb] >> 1) & 1, A.err, kErrTimeoutLoad);
             }
         }
     } else if (warp == 2) {
@@ -309,6 +308,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tcur_start<TT>(cp, tpref, A);
             uint32_t js = 0;                  // tiles whose S has been issued
             bool ok = true;
+            // testing hook: hold back the signal of the first S tile, so that the
+            // softmax's wait for it runs out (the failure path, without a fault)
+            const bool stall = stall_first_tile();
             // S_js: Q' of its run (buffer run & 1) times the K tile of ring slot js
             auto issue_s = [&]() -> bool {
                 const int slot = js % NK;
@@ -333,7 +335,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             tc_mma_f16_ss(tmem + C::COL_S, a_lo, b, idesc_s, 1u);
                         }
                     }
-                tc_commit(bar(B_SFULL));
+                if (!(stall && js == 0)) tc_commit(bar(B_SFULL));
                 tc_commit(bar(B_KEMPTY + slot));
                 if (cs.last) tc_commit(bar(B_QEMPTY + (cs.run & 1)));   // last S of the run
                 ++js;
@@ -368,8 +370,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             // all issued MMAs must retire before TMEM is released
             tc_commit(bar(B_TEARDOWN));
-            volatile int never = 0;
-            mbar_wait(bar(B_TEARDOWN), 0, &never, A.err, kErrTimeoutMma);
+            mbar_wait_drain(bar(B_TEARDOWN), 0, A.err, kErrTimeoutMma);
         }
     } else {
         // ------------------------------------------------------------ softmax (warp 0)
@@ -490,29 +491,33 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 m_used = m_new;
             }
             const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
-            uint32_t pw[64];                    // the P row: 128 f16 entries
-            float ls = 0.f;
+            // the P row: 128 f16 entries.  The row sum is taken over the rounded
+            // values the PV product multiplies (a convex combination of V rows)
+            uint32_t pw[64];
+            float ls0 = 0.f, ls1 = 0.f;
             if constexpr (NH == 1) {
 #pragma unroll
                 for (int t = 0; t < TT; t += 2) {
                     const float p0 = ex2_approx(s[t] - m_off), p1 = ex2_approx(s[t + 1] - m_off);
-                    ls += p0 + p1;
                     const __half2 h2 = __floats2half2_rn(p0, p1);
-                    pw[t / 2] = act ? *reinterpret_cast<const uint32_t*>(&h2) : 0u;
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(&h2);
+                    ls0 = add_f16_lo(ls0, w);
+                    ls1 = add_f16_hi(ls1, w);
+                    pw[t / 2] = act ? w : 0u;
                 }
             } else {
                 const int hp = gl >> 1;
 #pragma unroll
                 for (int t = 0; t < TT; ++t) {
                     const float p = ex2_approx(s[t] - m_off);
-                    ls += p;
                     const uint32_t h = __half_as_ushort(__float2half_rn(p));
+                    if (t & 1) ls1 = add_f16_lo(ls1, h); else ls0 = add_f16_lo(ls0, h);
                     const uint32_t word = act ? ((gl & 1) ? (h << 16) : h) : 0u;
 #pragma unroll
                     for (int w = 0; w < NH / 2; ++w) pw[t * (NH / 2) + w] = (w == hp) ? word : 0u;
                 }
             }
-            l_sum += ls;
+            l_sum += ls0 + ls1;
             if (rescale) {
                 // O must not be in flight while it is rescaled
                 if (!mbar_wait(bar(B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, A.err, kErrTimeoutMma)) { ok = false; break; }

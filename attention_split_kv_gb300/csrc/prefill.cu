@@ -107,36 +107,9 @@ struct PrefillCfg {
     static_assert(CTAS_PER_SM * TMEM_COLS <= 512, "TMEM per SM");
 };
 
-// Elements of every 8 in a P row whose exponential runs on the FMA pipe
-// (ex2_poly2) instead of the MUFU unit; the rest use ex2.approx.  Measured on
-// GB300 (the MUFU unit is far from saturated here): 0 of 8 is fastest for D=64
-// (33.4 us per launch for S=2304, 16 heads, against 35.5 at 2 of 8, 37.5 at
-// 3 of 8 and 41.7 at 4 of 8).
-constexpr int kPolyPerEight = 0;
-
 // A row whose exponentials against the running max sum to at most this (2 to the
 // lazy-rescale threshold) keeps them: no tile max needed.
 constexpr float kFastSumLimit = 256.0f;
-
-// 2^x on the FMA/ALU pipes: n = round(x) (added to the float 1.5*2^23 so that
-// the rounding lands n in the low mantissa bits), f = x - n in [-1/2, 1/2],
-// 2^f by a cubic minimax fit (relative error 7.5e-5, below the f16 rounding
-// of P; coefficients from fit_exp2_poly.py), then n is added to the exponent
-// field.  x is clamped at -125 so the exponent never underflows; such values
-// round to 0 in f16.  Two elements at a time, in packed f32x2 arithmetic.
-__device__ __forceinline__ float2 ex2_poly2(float2 x) {
-    x = make_float2(fmaxf(x.x, -125.0f), fmaxf(x.y, -125.0f));
-    const float2 magic = make_float2(12582912.0f, 12582912.0f);
-    const float2 y = fadd2(x, magic);
-    const float2 n = fadd2(y, make_float2(-12582912.0f, -12582912.0f));
-    const float2 f = fadd2(x, make_float2(-n.x, -n.y));
-    float2 p = ffma2(make_float2(5.517166906e-02f, 5.517166906e-02f), f,
-                     make_float2(2.426111222e-01f, 2.426111222e-01f));
-    p = ffma2(p, f, make_float2(6.932609855e-01f, 6.932609855e-01f));
-    p = ffma2(p, f, make_float2(9.999280735e-01f, 9.999280735e-01f));
-    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(y.x) << 23)),
-                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(y.y) << 23)));
-}
 
 // Per-warpgroup register budgets (all four warps of a warpgroup execute these).
 template <int N>
@@ -393,10 +366,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (leader && *abort_flag) {
                     // let copies already in flight land before the CTA's shared memory goes away
                     // (the stage's byte count covers every lane's boxes)
-                    volatile int never = 0;
-                    if (is_k) mbar_wait(bar(B_QFULL), 0, &never, args.err, kErrTimeoutLoad);
+                    if (is_k) mbar_wait_drain(bar(B_QFULL), 0, args.err, kErrTimeoutLoad);
                     for (int j = max(0, issued - NST); j < issued; ++j)
-                        mbar_wait(bar(b_full + (j % NST)), (j / NST) & 1, &never, args.err, kErrTimeoutLoad);
+                        mbar_wait_drain(bar(b_full + (j % NST)), (j / NST) & 1, args.err, kErrTimeoutLoad);
                 }
             }
         } else if (warp == C::MMA_WARP) {
@@ -405,6 +377,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 constexpr uint32_t idesc_s = idesc_f16_f32(BM, BN, false);
                 constexpr uint32_t idesc_o = idesc_f16_f32(BM, D, true);
                 bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, args.err, kErrTimeoutLoad);
+                // testing hook: hold back the signal of the first S tile, so that the
+                // softmax's wait for it runs out (the failure path, without a fault)
+                const bool stall = stall_first_tile();
                 auto issue_s = [&](int j) {
                     const int st = j % C::KST;
                     const uint32_t d_tmem = tmem + (j % NBUF) * BN;
@@ -418,7 +393,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             tc_mma_f16_ss(d_tmem, a, b, idesc_s, (c | kk) != 0);
                         }
                     }
-                    tc_commit(bar(B_SFULL + (j % NBUF)));
+                    if (!(stall && j == 0)) tc_commit(bar(B_SFULL + (j % NBUF)));
                     tc_commit(bar(B_KEMPTY + st));
                 };
                 if (ok && n_tiles > 0) {
@@ -455,8 +430,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 // all issued MMAs must retire before TMEM is released
                 tc_commit(bar(B_TEARDOWN));
-                volatile int never = 0;
-                mbar_wait(bar(B_TEARDOWN), 0, &never, args.err, kErrTimeoutMma);
+                mbar_wait_drain(bar(B_TEARDOWN), 0, args.err, kErrTimeoutMma);
             }
         }
     } else {
@@ -576,11 +550,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             };
             const float2 sl2 = make_float2(scale_log2, scale_log2);
             const uint32_t p_addr = lane_base + C::COL_P + (j % NBUF) * C::P_COLS + ch * (CW / 2);
-            // p = 2^(t*scale - m_off) (or 2^(t - m_off)) in packed f32x2 arithmetic, packed to
-            // f16 and stored to TMEM 32 elements at a time; returns the row's sum of p
+            // p = 2^(t*scale - m_off) (or 2^(t - m_off)) in packed f32x2 arithmetic, rounded to
+            // f16 and stored to TMEM 32 elements at a time; returns the row's sum of the
+            // ROUNDED p, the values the PV product multiplies, so that the output is a
+            // convex combination of V rows (one dominant key gives its V row exactly)
             auto exps = [&](float m_off) -> float {
-                float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                make_float2(0.f, 0.f)};   // independent partial sums (short dependency chains)
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // independent partial sums
                 const float2 nm2 = make_float2(-m_off, -m_off);
 #pragma unroll
                 for (int c = 0; c < CW / 32; ++c) {
@@ -589,16 +564,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     for (int i = 0; i < 32; i += 2) {
                         const float2 ti = make_float2(t[c * 32 + i], t[c * 32 + i + 1]);
                         const float2 x = MODE == kModeRaw ? ffma2(ti, sl2, nm2) : fadd2(ti, nm2);
-                        const bool poly = (i & 7) < kPolyPerEight;
-                        const float2 p = poly ? ex2_poly2(x) : make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                         const __half2 hp = __floats2half2_rn(p.x, p.y);
-                        ls[(i / 2) & 3] = fadd2(ls[(i / 2) & 3], p);
                         packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+                        const int a = (i / 2) & 3;
+                        ls[2 * a] = add_f16_lo(ls[2 * a], packed[i / 2]);
+                        ls[2 * a + 1] = add_f16_hi(ls[2 * a + 1], packed[i / 2]);
                     }
                     tc_st_32x32b_x16(p_addr + c * 16, packed);
                 }
-                const float2 lsum2 = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
-                return lsum2.x + lsum2.y;
+                return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
             };
             // Optimistic pass (D=128, whole rows): exponentials against the running max,
             // without the tile's max.  A row whose p sum to at most 2^8 has every p <= 2^8,
@@ -794,6 +769,13 @@ attn_status launch_prefill_dm(const PrefillLaunch& L) {
     a.lpt = PAGED && n_pairs <= kLptMaxPairs;
     const dim3 grid = !PAGED ? dim3((L.S + BM - 1) / BM, L.Hq)
                       : a.lpt ? dim3(n_pairs * L.Hq) : dim3(a.max_qt, L.Hq, L.B);
+    if (trace_enabled())
+        trace("prefill_tc_kernel<D=%d,mode=%s,paged=%d> grid=(%u,%u,%u) block=%d smem=%u tmem_cols=%u "
+              "ctas_per_sm=%d key_tile=%d S=%d Hq=%d Hkv=%d causal=%d window=%d softcap=%g scale=%g%s",
+              D, MODE == kModeRaw ? "raw" : MODE == kModeScaled ? "scaled" : "capped", (int)PAGED, grid.x, grid.y,
+              grid.z, C::THREADS, C::SMEM_ALLOC, C::TMEM_COLS, C::CTAS_PER_SM, C::BN, PAGED ? L.total_q : L.S,
+              L.Hq, L.Hkv, L.causal, L.window, L.softcap, L.scale,
+              PAGED ? (a.lpt ? " order=longest-first" : " order=(tile,head,seq)") : "");
     prefill_tc_kernel<D, MODE, PAGED><<<grid, C::THREADS, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
@@ -821,6 +803,14 @@ attn_status launch_prefill_p(const PrefillLaunch& L) {
 
 attn_status launch_prefill(const PrefillLaunch& L) {
     return L.paged ? launch_prefill_p<true>(L) : launch_prefill_p<false>(L);
+}
+
+// Sets this translation unit's test controls (see ptx.cuh).
+attn_status set_test_controls_prefill(unsigned long long wait_limit_ns, int stall) {
+    if (cudaMemcpyToSymbol(g_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_stall_first_tile, &stall, sizeof(stall)) != cudaSuccess)
+        return set_error(ATTN_ECUDA, "test controls (prefill): %s", cudaGetErrorString(cudaGetLastError()));
+    return ATTN_OK;
 }
 
 }  // namespace attn

@@ -57,6 +57,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Test controls of the translation unit that includes this header (each has
+// its own copy, set through the library's testing hook): the time limit of
+// pipeline waits, and a stall of the first tile's signal, which makes one
+// pipeline wait of every CTA run out so that the failure path can be tested
+// without a fault.  Waits for copies already in flight (mbar_wait_drain)
+// always keep the full limit.
+static __device__ unsigned long long g_wait_limit_ns = kWaitTimeoutNs;
+static __device__ int g_stall_first_tile = 0;
+
+__device__ __forceinline__ bool stall_first_tile() {
+    return *static_cast<volatile int*>(&g_stall_first_tile) != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false if
 // another role raised the CTA's abort flag or the time limit passed (then
 // this role raises the abort flag and records `code`).
@@ -64,15 +77,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           int* err_word, int code) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
+    const uint64_t limit = *static_cast<volatile unsigned long long*>(&g_wait_limit_ns);
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs) {
+            if (globaltimer() - t0 > limit) {
                 *abort_flag = 1;
                 atomicExch(err_word, code);
                 return false;
             }
+        }
+    }
+}
+
+// Wait for copies or tensor-core work already in flight to land before the
+// CTA's shared memory or tensor memory goes away (after an abort): no abort
+// flag, and always the full time limit.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* err_word, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0 && globaltimer() - t0 > kWaitTimeoutNs) {
+            atomicExch(err_word, code);
+            return false;
         }
     }
 }
@@ -265,6 +294,18 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     return upk(d);
 }
 
+
+// acc + the f16 value in the low (high) half of w, one f32 rounding (the
+// sm_100-family mixed-precision add: the f16 operand widens exactly).  Used to
+// sum P over exactly the f16 values the PV product multiplies.
+__device__ __forceinline__ float add_f16_lo(float acc, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %0;\n\t}" : "+f"(acc) : "r"(w));
+    return acc;
+}
+__device__ __forceinline__ float add_f16_hi(float acc, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %0;\n\t}" : "+f"(acc) : "r"(w));
+    return acc;
+}
 
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

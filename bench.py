@@ -13,9 +13,12 @@ masks, online softmax, PV, split combine, tensor-core prefill tiles):
   ring_window_decode   B=32, 32q/8kv heads, D=128, 4096-slot ring, logical kv_len 4K..64K
   tiered_int8_decode   B=32, 32q/8kv heads, D=128, int8 paged cold tier 2K..16K + f16 1024-slot hot ring, f32 q
   paged_decode_f32io   paged_gqa_decode's shape and lengths with f32 queries and f32 outputs
+  tiny_decode          B=1, 4q/2kv heads, D=64, kv_len 128: launch latency, reported in us
 
 The headline metric is the vision workload's TFLOP/s (algorithmic FLOPs
 4*S^2*D*H over the call's CUDA-event time); decode workloads report KV GB/s.
+Every workload also carries the fp64 CPU oracle timed on a bounded sample of
+its own rows, credited at the workload's algorithmic work per row.
 Inputs are resident in HBM; L2 is flushed before every timed call, outside the
 timed events: a 256 MiB write, then a 256 MiB read of another buffer so that the
 write's dirty lines are not written back during the timed call.  `e2e` repeats the headline through the same
@@ -61,7 +64,14 @@ NCU_TRAFFIC = {
 }
 METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
 WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode",
-                  "chunked_prefill_paged", "ring_window_decode", "tiered_int8_decode", "paged_decode_f32io"]
+                  "chunked_prefill_paged", "ring_window_decode", "tiered_int8_decode", "paged_decode_f32io",
+                  "tiny_decode"]
+# workloads bound by launch latency: reported as microseconds per call (lower is better)
+LATENCY_WORKLOADS = {"tiny_decode"}
+# Nominal GB300 figures, for the second fraction of each roofline: HBM3e
+# bandwidth and the dense f16/bf16 tensor-core rate.  The fraction the targets
+# are judged on is the one against the measured peaks (`frac`).
+SPEC_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 L2_FLUSH_BYTES = 256 << 20
 HOST_SLACK_CYCLES = 200_000   # about 0.1 ms of device time before each timed call
 
@@ -75,6 +85,15 @@ def load_peaks():
                 "source": "measured"}
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def rows_total(case):
+    """Output rows of a workload: (sequence, head), (query, head) or (chunk row, head)."""
+    if hasattr(case, "q_lens"):
+        return case.total_q * case.n_heads
+    if hasattr(case, "seq_len"):
+        return case.seq_len * case.n_heads
+    return case.batch * case.n_heads
 
 
 # ---------------------------------------------------------------- algorithmic work
@@ -274,31 +293,64 @@ def barrier(world):
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def oracle_sample_rate(case, n_rows, seed=0):
-    """Time the oracle on n_rows sampled (query, head) rows of a prefill case.
-
-    Returns (TFLOP/s credited at the workload's per-row algorithmic FLOPs,
-    seconds, threads)."""
+def _sample_rows(case, n_rows, seed):
     import numpy as np
-    import oracle
     rng = np.random.default_rng(seed)
-    rows = [(int(rng.integers(case.seq_len)), int(rng.integers(case.n_heads))) for _ in range(n_rows)]
-    per_row = prefill_flops(case) / (case.seq_len * case.n_heads)
+    if hasattr(case, "q_lens"):
+        outer = case.total_q
+    elif hasattr(case, "seq_len"):
+        outer = case.seq_len
+    else:
+        outer = case.batch
+    return [(int(rng.integers(outer)), int(rng.integers(case.n_heads))) for _ in range(n_rows)]
+
+
+def _oracle_call(kind, case, rows, n_threads=0):
+    import oracle
+    if kind == "decode":
+        return oracle.decode(case, rows=rows, n_threads=n_threads)
+    if kind == "tiered":
+        return oracle.decode_tiered(case, rows=rows, n_threads=n_threads)
+    if kind == "chunked":
+        return oracle.prefill_paged(case, rows=rows, n_threads=n_threads)
+    return oracle.prefill(case, rows=rows, n_threads=n_threads)
+
+
+def oracle_sample_rate(kind, case, amount, scale, n_rows, seed=0):
+    """Time the oracle on n_rows sampled output rows of a workload.
+
+    Returns (rate credited at the workload's algorithmic work per row, in the
+    workload's unit (amount / scale per second), seconds, threads)."""
+    import oracle
+    rows = _sample_rows(case, n_rows, seed)
+    per_row = amount / rows_total(case)
     t0 = time.perf_counter()
-    oracle.prefill(case, rows=rows)
+    _oracle_call(kind, case, rows)
     dt = time.perf_counter() - t0
-    return per_row * n_rows / dt / 1e12, dt, oracle.max_threads()
+    return per_row * n_rows / dt / scale, dt, oracle.max_threads()
 
 
-def cpu_baseline(case, target_s=12.0):
-    """Bounded oracle sample (about target_s seconds) of the headline workload."""
-    probe = 64
-    _, dt, _ = oracle_sample_rate(case, probe, seed=1)
-    n = int(min(case.seq_len * case.n_heads, max(probe, probe * target_s / max(dt, 1e-6))))
-    rate, dt, threads = oracle_sample_rate(case, n, seed=2)
-    return {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": "%d of %d (query, head) rows of %s, %.1f s" % (n, case.seq_len * case.n_heads,
-                                                                    HEADLINE, dt)}
+def cpu_baseline(name, kind, case, amount, unit, target_s):
+    """Bounded oracle sample (about target_s seconds) of one workload."""
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    probe = 8
+    _, dt, _ = oracle_sample_rate(kind, case, amount, scale, probe, seed=1)
+    n = int(min(rows_total(case), max(probe, probe * target_s / max(dt, 1e-6))))
+    rate, dt, threads = oracle_sample_rate(kind, case, amount, scale, n, seed=2)
+    return {"value": rate, "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": "%d of %d output rows of %s, %.1f s" % (n, rows_total(case), name, dt)}
+
+
+def cpu_latency(case, n_threads, min_s=1.0):
+    """Oracle time of one whole call of a small decode case, in microseconds."""
+    import oracle
+    reps, t = 0, 0.0
+    t0 = time.perf_counter()
+    while t < min_s or reps < 3:
+        oracle.decode(case, n_threads=n_threads)
+        reps += 1
+        t = time.perf_counter() - t0
+    return 1e6 * t / reps, reps
 
 
 def run_reference(args, rank, world):
@@ -309,16 +361,17 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     case = si.make_workload(HEADLINE, device="cpu")
-    probe_rate, probe_dt, _ = oracle_sample_rate(case, 32, seed=0)
+    amount = prefill_flops(case)
+    probe_rate, probe_dt, _ = oracle_sample_rate("prefill", case, amount, 1e12, 32, seed=0)
     budget_per_step = 150.0 / max(1, args.steps + args.warmup)
     rows = int(max(16, min(case.seq_len * case.n_heads, 32 * budget_per_step / max(probe_dt, 1e-6))))
     for w in range(args.warmup):
-        oracle_sample_rate(case, rows, seed=100 + w)
+        oracle_sample_rate("prefill", case, amount, 1e12, rows, seed=100 + w)
     total_t, flops = 0.0, 0.0
-    per_row = prefill_flops(case) / (case.seq_len * case.n_heads)
+    per_row = amount / rows_total(case)
     threads = oracle.max_threads()
     for k in range(args.steps):
-        _, dt, threads = oracle_sample_rate(case, rows, seed=1000 + k)
+        _, dt, threads = oracle_sample_rate("prefill", case, amount, 1e12, rows, seed=1000 + k)
         total_t += dt
         flops += per_row * rows
     value = flops / total_t / 1e12
@@ -503,19 +556,26 @@ def main(argv=None):
     for n in names:
         unit, amount, bound, launches = work[n]
         t_ms = max_over_ranks(ms[n], world)
+        if n in LATENCY_WORKLOADS:
+            # launch-latency bound: microseconds per call (the slowest rank's), no roofline
+            results[n] = {"value": 1000.0 * t_ms, "unit": "us", "higher_is_better": False, "ms": t_ms,
+                          "launches_per_call": launches,
+                          "roofline": {"bound": "latency", "achieved": None, "peak": None, "unit": None,
+                                       "frac": None, "traffic": None,
+                                       "note": "%d KB of KV: the call's cost is launch latency, not bytes"
+                                               % (amount // 1000)}}
+            continue
         total = sum_over_ranks(amount, world)
-        if unit == "GB/s":
-            value = total / (t_ms * 1e-3) / 1e9
-            per_gpu = amount / (ms[n] * 1e-3) / 1e9
-            peak = peaks["hbm_gbs"]
-        else:
-            value = total / (t_ms * 1e-3) / 1e12
-            per_gpu = amount / (ms[n] * 1e-3) / 1e12
-            peak = peaks["bf16_tflops"]
+        key = "hbm_gbs" if unit == "GB/s" else "bf16_tflops"
+        div = 1e9 if unit == "GB/s" else 1e12
+        value = total / (t_ms * 1e-3) / div
+        per_gpu = amount / (ms[n] * 1e-3) / div
+        peak = peaks[key]
         results[n] = {"value": value, "unit": unit, "ms": t_ms, "launches_per_call": launches,
                       "roofline": {"bound": bound, "achieved": per_gpu, "peak": peak,
                                    "unit": unit, "frac": per_gpu / peak, "traffic": NCU_TRAFFIC.get(n),
                                    "peak_source": peaks["source"],
+                                   "frac_spec": per_gpu / SPEC_PEAKS[key], "peak_spec": SPEC_PEAKS[key],
                                    "scope": "whole call" if launches > 1 else "single kernel"}}
     if rank != 0:
         return 0
@@ -550,10 +610,29 @@ def main(argv=None):
         "device_status": "ok" if status == 0 else "error %d" % status,
     }
     line["roofline"]["kernel"] = "prefill_tc_kernel<64>" if head_name == HEADLINE else head_name
-    if world == 1 and not args.no_cpu_baseline and head_name == HEADLINE:
+    if world == 1 and not args.no_cpu_baseline:
+        # the fp64 oracle on the host cores, on a bounded sample of each workload
         import oracle
         oracle.build()
-        line["cpu_baseline"] = cpu_baseline(cases[HEADLINE].to("cpu"))
+        all_threads = oracle.max_threads()
+        for n in names:
+            unit, amount, _, _ = work[n]
+            kind = si.WORKLOADS[n]["kind"]
+            cpu = cases[n].to("cpu")
+            if n in LATENCY_WORKLOADS:
+                us_all, reps = cpu_latency(cpu, all_threads)
+                us_one, reps1 = cpu_latency(cpu, 1)
+                oracle.decode(cpu, n_threads=all_threads)   # the thread count is sticky: restore it
+                results[n]["cpu_baseline"] = {
+                    "value": us_all, "unit": "us", "cores": all_threads, "kind": "oracle",
+                    "value_1core": us_one, "sample": "the whole call, %d (all cores) and %d (1 core) repetitions"
+                                                    % (reps, reps1)}
+            else:
+                results[n]["cpu_baseline"] = cpu_baseline(n, kind, cpu, amount, unit,
+                                                          12.0 if n == HEADLINE else 3.0)
+            del cpu
+        if head_name in results and "cpu_baseline" in results[head_name]:
+            line["cpu_baseline"] = results[head_name]["cpu_baseline"]
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -165,10 +165,18 @@ attn_status attn_decode_ring(const void* q, const void* k_ring, const void* v_ri
  * attn_decode_ex -- attn_decode with every cache layout and the query and
  * output element types as arguments.
  *
- *  q, q_dtype      device [B, Hq, D] of ATTN_F16 or ATTN_F32.  f32 queries keep
- *                    their precision: the tensor-core kernel multiplies two f16
- *                    terms hi + lo (hi = f16(q), lo = f16(q - hi)) into one
- *                    accumulator; the CUDA-core kernel reads them as f32.
+ *  q, q_dtype      device [B, Hq, D] of ATTN_F16 or ATTN_F32.  How far f32
+ *                    queries keep their precision depends on the cache:
+ *                    f16 caches with D 64/128 (tensor-core kernel) multiply two
+ *                    f16 terms hi + lo (hi = f16(q), lo = f16(q - hi), together
+ *                    within 2^-22 |q|) into one accumulator; f16 caches with
+ *                    D 256 or pages of fewer than 16 tokens read q as f32.
+ *                    int8 caches round every query (f16 or f32) to 16-bit fixed
+ *                    point with one scale per (sequence, head), 1/32767 of that
+ *                    head's largest |q| (error at most max|q| / 65534 per
+ *                    element), so that q.k is an exact integer dot product of
+ *                    the codes: there f32 queries are no more precise than
+ *                    that rounding.
  *  ring_size       > 0 selects the ring layout of attn_decode_ring (kv_len is
  *                    then the logical length, page_table must be NULL and max_kv
  *                    is ignored); 0 selects attn_decode's contiguous or paged
@@ -352,6 +360,30 @@ attn_status attn_decode_validate(const int32_t* kv_len, const int32_t* page_tabl
  * a page id outside the pool, else ATTN_OK.
  */
 attn_status attn_device_status(void* stream);
+
+/*
+ * attn_testing_set_waits -- testing hook for the failure path of the kernels'
+ * bounded waits; not for production use.  (The source pages have no
+ * counterpart: their WebGPU host code throws on errors and has no device-side
+ * waits.)  Every pipeline wait of the kernels (a tile's copy, a tensor-core
+ * result, a free buffer) gives up after a time limit, records a code in the
+ * library's device error word, raises the CTA's abort flag so that every role
+ * leaves its loop, waits (with the full limit) for its own copies and
+ * tensor-core work already in flight, frees its tensor memory and returns.
+ *
+ *  wait_limit_ns     the time limit of pipeline waits in ns; 0 restores the
+ *                      default (4 s).  Waits for work already in flight keep
+ *                      the default.
+ *  stall_first_tile  1: from now on every CTA of the prefill and tensor-core
+ *                      decode kernels holds back the signal that its first
+ *                      S tile is ready, and the CUDA-core decode kernel issues
+ *                      no copy, so one pipeline wait of every CTA runs out:
+ *                      the call's output is invalid and attn_device_status
+ *                      then returns ATTN_ETIMEOUT.  0: normal operation.
+ *  The settings apply to the current device and to every later launch; the
+ *  call is synchronous.  Returns ATTN_EINVAL for another stall value.
+ */
+attn_status attn_testing_set_waits(unsigned long long wait_limit_ns, int stall_first_tile);
 
 #ifdef __cplusplus
 }

@@ -2,13 +2,16 @@
 
 Tolerances (fixed by the target statement of the path): f16 K/V outputs must
 match the fp64 oracle to max-abs <= 2e-3 and relative L2 <= 1e-3; int8 K/V
-outputs to relative L2 <= 5e-3 against the oracle run on the dequantised
-values (the oracle dequantises from the same codes and scales).
+outputs to 5e-3 against the oracle run on the dequantised values (the oracle
+dequantises from the same codes and scales).  The int8 figure stands in the
+target beside both the max-abs and the relative-L2 bound, so both are applied:
+max-abs <= 5e-3 and relative L2 <= 5e-3.
 """
 import numpy as np
 
 F16_MAX_ABS = 2e-3
 F16_REL_L2 = 1e-3
+INT8_MAX_ABS = 5e-3
 INT8_REL_L2 = 5e-3
 LSE_MAX_ABS = 2e-3
 
@@ -25,11 +28,9 @@ def errors(got, ref):
 def assert_close(got, ref, int8=False, what=""):
     max_abs, rel = errors(got, ref)
     assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), "%s: non-finite output" % what
-    if int8:
-        assert rel <= INT8_REL_L2, "%s: rel-L2 %.3g > %.3g (max-abs %.3g)" % (what, rel, INT8_REL_L2, max_abs)
-    else:
-        assert max_abs <= F16_MAX_ABS and rel <= F16_REL_L2, \
-            "%s: max-abs %.3g (<= %.3g), rel-L2 %.3g (<= %.3g)" % (what, max_abs, F16_MAX_ABS, rel, F16_REL_L2)
+    tol_abs, tol_rel = (INT8_MAX_ABS, INT8_REL_L2) if int8 else (F16_MAX_ABS, F16_REL_L2)
+    assert max_abs <= tol_abs and rel <= tol_rel, \
+        "%s: max-abs %.3g (<= %.3g), rel-L2 %.3g (<= %.3g)" % (what, max_abs, tol_abs, rel, tol_rel)
 
 
 def assert_lse_close(got, ref, what=""):

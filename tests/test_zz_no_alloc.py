@@ -2,8 +2,10 @@
 (an engine plugin with no allocator, a decode loop that must never call
 cudaMalloc).  It takes its scratch from a fixed device array inside the
 library, so its results must equal those of attn_decode given a caller
-workspace.  This file is collected last on purpose: it runs after every other
-test and also alone in a fresh process."""
+workspace.  This file is collected last (its name sorts after every other test
+file), so a run that stops at the first failure has run everything else first;
+it needs no state from earlier tests and also passes alone in a fresh process:
+python -m pytest tests/test_zz_no_alloc.py -m gpu"""
 import numpy as np
 import pytest
 import torch
@@ -37,6 +39,26 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
         torch.cuda.synchronize()
         assert_close(out.float().cpu().numpy(), ref.double().cpu().numpy(), int8=g.int8, what="noalloc")
         assert np.allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), atol=2e-3, rtol=0, equal_nan=False)
+    assert attn.attn_device_status() == attn.ATTN_OK
+
+
+def test_noalloc_smaller_call_after_a_larger_one():
+    # every call shares the one scratch array, which keeps the previous call's
+    # contents: a smaller call (same head_dim and layout) after a larger one must
+    # still read only what it wrote itself
+    attn.load()
+    big = si.make_decode_case(8, 32, 8, 128, (2000, 4900), seed=311, page_size=16).to("cuda")
+    small = si.make_decode_case(2, 8, 2, 128, [300, 1200], seed=312, page_size=16).to("cuda")
+    out_big = torch.empty((big.batch, big.n_heads, big.head_dim), dtype=torch.float16, device="cuda")
+    _noalloc(big, out_big, None)
+    ref_lse = torch.empty((small.batch, small.n_heads), dtype=torch.float32, device="cuda")
+    ref = attn.decode(small, lse_out=ref_lse)
+    out = torch.full_like(ref, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    _noalloc(small, out, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert torch.equal(lse, ref_lse)
     assert attn.attn_device_status() == attn.ATTN_OK
 
 
