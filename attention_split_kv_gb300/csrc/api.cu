@@ -427,6 +427,8 @@ attn_status attn_prefill(const void* q, const void* k, const void* v, int seq_le
         return set_error(ATTN_EINVAL, "attn_prefill: n_heads (%d) must be a multiple of n_kv_heads (%d)", n_heads,
                          n_kv_heads);
     if (n_heads > 65535) return set_error(ATTN_EUNSUPPORTED, "attn_prefill: n_heads above 65535");
+    if ((seq_len + 127) / 128 > 65535)
+        return set_error(ATTN_EUNSUPPORTED, "attn_prefill: seq_len above %d", 65535 * 128);
     if (head_dim != 64 && head_dim != 128 && head_dim != 256)
         return set_error(ATTN_EUNSUPPORTED, "attn_prefill: head_dim %d not supported (64, 128, 256)", head_dim);
     if (window < 0) return set_error(ATTN_EINVAL, "attn_prefill: window must be >= 0 (0 = off)");

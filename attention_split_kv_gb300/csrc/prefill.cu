@@ -204,7 +204,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         jt0_ = lo_ / BN;
         return hi_ > lo_ ? (hi_ + BN - 1) / BN - jt0_ : 0;
     };
-    int n_q = args.S, L = args.S, pos0 = 0, q_base = 0, b = 0, qt = 0, h = blockIdx.y;
+    // contiguous prefill: heads fastest (x), query tiles (y), so that the longest
+    // causal tiles of every head launch first; paged chunks set these below
+    int n_q = args.S, L = args.S, pos0 = 0, q_base = 0, b = 0, qt = 0, h = blockIdx.x;
     if constexpr (PAGED) {
         auto chunk_of = [&](int bb, int& qs, int& nq, int& Lb, int& p0) {
             qs = args.q_start[bb];
@@ -246,14 +248,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             h = static_cast<int>(blockIdx.x) % args.Hq;
         } else {
             b = blockIdx.z;
+            h = blockIdx.y;
             qt = static_cast<int>(gridDim.x - 1 - blockIdx.x);
         }
         chunk_of(b, q_base, n_q, L, pos0);
     }
     const int n_qt = (n_q + BM - 1) / BM;
     // causal tiles late in the sequence carry the most keys: launch them first
-    if constexpr (!PAGED)
-        qt = args.causal ? (n_qt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    if constexpr (!PAGED) qt = args.causal ? (n_qt - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
     if (PAGED && qt >= n_qt) return;   // a shorter chunk: no queries for this CTA
     const int g = h / (args.Hq / args.Hkv);
     const int q0 = qt * BM;
@@ -673,20 +675,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             __half* orow = args.out + (static_cast<size_t>(q_base + qi) * args.Hq + h) * D;
 #pragma unroll 1
             for (int c = 0; c < OW / 32; ++c) {
-                uint32_t r[32];
+                float o[32];
                 if (n_tiles > 0) {
+                    uint32_t r[32];
                     tc_ld_32x32b_x32(lane_base + C::COL_O + ch * OW + c * 32, r);
                     tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]) * inv_l;
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = 0u;   // no key at all: O was never written
+                    for (int i = 0; i < 32; ++i) o[i] = 0.f;   // no key at all: O was never written
                 }
                 if (row_ok) {
                     uint32_t hv[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const __half2 p2 = __floats2half2_rn(__uint_as_float(r[2 * i]) * inv_l,
-                                                             __uint_as_float(r[2 * i + 1]) * inv_l);
+                        const __half2 p2 = __floats2half2_rn(o[2 * i], o[2 * i + 1]);
                         hv[i] = *reinterpret_cast<const uint32_t*>(&p2);
                     }
                     uint4* dst = reinterpret_cast<uint4*>(orow + ch * OW + c * 32);
@@ -767,7 +771,8 @@ attn_status launch_prefill_dm(const PrefillLaunch& L) {
     a.max_qt = PAGED ? (L.max_q + BM - 1) / BM : 0;
     const int n_pairs = L.B * a.max_qt;
     a.lpt = PAGED && n_pairs <= kLptMaxPairs;
-    const dim3 grid = !PAGED ? dim3((L.S + BM - 1) / BM, L.Hq)
+    // contiguous: heads fastest, then query tiles (longest first when causal)
+    const dim3 grid = !PAGED ? dim3(L.Hq, (L.S + BM - 1) / BM)
                       : a.lpt ? dim3(n_pairs * L.Hq) : dim3(a.max_qt, L.Hq, L.B);
     if (trace_enabled())
         trace("prefill_tc_kernel<D=%d,mode=%s,paged=%d> grid=(%u,%u,%u) block=%d smem=%u tmem_cols=%u "
@@ -775,7 +780,8 @@ attn_status launch_prefill_dm(const PrefillLaunch& L) {
               D, MODE == kModeRaw ? "raw" : MODE == kModeScaled ? "scaled" : "capped", (int)PAGED, grid.x, grid.y,
               grid.z, C::THREADS, C::SMEM_ALLOC, C::TMEM_COLS, C::CTAS_PER_SM, C::BN, PAGED ? L.total_q : L.S,
               L.Hq, L.Hkv, L.causal, L.window, L.softcap, L.scale,
-              PAGED ? (a.lpt ? " order=longest-first" : " order=(tile,head,seq)") : "");
+              PAGED ? (a.lpt ? " order=longest-first" : " order=(tile,head,seq)")
+                    : L.causal ? " order=heads fastest, longest query tiles first" : " order=heads fastest");
     prefill_tc_kernel<D, MODE, PAGED><<<grid, C::THREADS, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));

@@ -290,7 +290,8 @@ attn_status attn_decode_noalloc(const void* q, const void* k_cache, const void* 
  *  window  W > 0: causal keeps i - W < j <= i; bidirectional keeps |i - j| < W.
  *  softcap, scale  as in attn_decode.
  *  out   device f16 [S, Hq, D].   lse_out  device f32 [S, Hq] or NULL.
- *  D must be 64, 128 or 256.  Base addresses must be 16-byte aligned.
+ *  D must be 64, 128 or 256; seq_len at most 65535 * 128.  Base addresses
+ *  must be 16-byte aligned.
  */
 attn_status attn_prefill(const void* q, const void* k, const void* v,
                          int seq_len, int n_heads, int n_kv_heads, int head_dim,

@@ -19,6 +19,7 @@ attn.build(); attn.load()
 attn.prefill(si.make_prefill_case(200, 4, 2, 64, seed=1, causal=True).to("cuda"))
 attn.decode(si.make_decode_case(2, 8, 2, 128, [300, 40], seed=2, page_size=16).to("cuda"))
 attn.decode(si.make_decode_case(2, 8, 2, 128, [300, 40], seed=3, int8=True).to("cuda"))
+attn.prefill(si.make_prefill_case(2560, 8, 4, 256, seed=4, causal=True).to("cuda"))
 torch.cuda.synchronize()
 assert attn.attn_device_status() == attn.ATTN_OK
 """
@@ -38,11 +39,13 @@ def _run(env_value):
 def test_trace_describes_every_launch():
     lines = _run("1")
     text = "\n".join(lines)
-    assert "prefill_tc_kernel<D=64,mode=raw,paged=0> grid=(2,4,1)" in text, text
+    assert "prefill_tc_kernel<D=64,mode=raw,paged=0> grid=(4,2,1)" in text, text
     assert "decode_tc_kernel<D=128,NH=2,f32q=0>" in text and "layout=paged" in text, text
     assert "decode_split_kernel<D=128,int8=1,GH=4>" in text and "layout=contiguous" in text, text
     assert text.count("decode_combine_kernel<D=128,tiers=1,out=f16>") == 2, text
-    assert len(lines) == 5, text
+    assert "prefill_tc_kernel<D=256,mode=raw,paged=0> grid=(8,20,1)" in text, text
+    assert "order=heads fastest, longest query tiles first" in text, text
+    assert len(lines) == 6, text
 
 
 def test_trace_is_off_by_default():
