@@ -109,7 +109,7 @@ struct DecodePlan {
     int split;         // keys per split (multiple of 16)
     long max_items;    // upper bound of work items (sequence, head block, split)
     int n_fix;         // fix-up slots: one per CTA of the balanced kernel (the most it may launch)
-    size_t off_tpref, off_fix_meta, off_lse, off_fix_lse, off_o, off_fix_o, off_qsplit, bytes;
+    size_t off_tpref, off_fix_meta, off_lse, off_fix_lse, off_o, off_fix_o, bytes;
 };
 bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys, DecodePlan* plan);
 attn_status launch_decode(const DecodeLaunch& L, const DecodePlan& plan);

@@ -657,18 +657,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
 #include "decode_tc.cuh"
 
-// f32 queries for the tensor-core kernel: q = hi + lo with hi = f16(q) and
-// lo = f16(q - hi) (RNE both), so hi + lo matches q to about 2^-22 of |q|;
-// hi goes to rows [0, B) of a [2B, Hq, D] f16 array and lo to rows [B, 2B).
-__global__ void q_split_kernel(const float* __restrict__ q, __half* __restrict__ hl, long n) {
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-        const float x = q[i];
-        const __half hi = __float2half_rn(x);
-        hl[i] = hi;
-        hl[n + i] = __float2half_rn(x - __half2float(hi));
-    }
-}
-
 // One tier of the combine: where a split kernel left its partials, and the
 // range arguments that say which items it wrote.
 struct CombTier {
@@ -960,33 +948,14 @@ int decode_grid(const DecodePlan& plan) {
 }
 
 // Tensor-core split kernel: f16 caches, head_dim 64/128, boxes of 16 rows x NH heads.
-// Q2: f32 queries, split into f16 hi and lo terms in the workspace first.
+// Q2: f32 queries (split into f16 hi and lo terms by the kernel as it loads them).
 template <int D, int NH, bool Q2>
 attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, SplitOut* so) {
     using C = tcdec::Cfg<D, Q2>;
     const bool paged = L.page_table != nullptr;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tk, tv;
     attn_status st;
     const int q_rows = L.Hq < tcdec::QROWS ? L.Hq : tcdec::QROWS;
-    const void* qsrc = L.q;
-    if constexpr (Q2) {
-        __half* hl = reinterpret_cast<__half*>(static_cast<uint8_t*>(L.workspace) + plan.off_qsplit);
-        const long n = (long)L.B * L.Hq * D;
-        const int blocks = (int)((n + 255) / 256 < 4 * sm_count() ? (n + 255) / 256 : 4 * sm_count());
-        if (trace_enabled()) trace("q_split_kernel grid=%d block=256 (f32 q -> f16 hi + lo)", blocks);
-        q_split_kernel<<<blocks, 256, 0, L.stream>>>(static_cast<const float*>(L.q), hl, n);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return set_error(ATTN_ECUDA, "q split launch failed: %s", cudaGetErrorString(e));
-        qsrc = hl;
-    }
-    {
-        // q [B][Hq][D] (Q2: [2B][Hq][D], hi then lo): boxes of (64 dims, q_rows heads, 1), 128-byte swizzle
-        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)L.Hq, (uint64_t)L.B * (Q2 ? 2 : 1)};
-        const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * L.Hq};
-        const uint32_t box[3] = {64u, (uint32_t)q_rows, 1u};
-        if ((st = encode_tmap_sw128(&tq, qsrc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, dims, strides, box)) != ATTN_OK)
-            return st;
-    }
     {
         // [pages or B][rows][Hkv][D]: boxes of (64 dims, NH heads, 16 rows, 1), 128-byte swizzle
         uint64_t dims[4], strides[3];
@@ -1022,7 +991,7 @@ attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, Spli
               D, NH, (int)Q2, grid, tcdec::kThreads, C::SMEM_ALLOC, L.B, L.Hq, L.Hkv,
               paged ? "paged" : L.ring > 0 ? "ring" : "contiguous", L.tier, plan.split, plan.n_hb, a.U,
               plan.max_items, tcdec::TR / NH, C::NK, C::NV);
-    tcdec::decode_tc_kernel<D, NH, Q2><<<grid, tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a, q_rows);
+    tcdec::decode_tc_kernel<D, NH, Q2><<<grid, tcdec::kThreads, C::SMEM_ALLOC, L.stream>>>(tk, tv, a, q_rows);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode tc launch failed: %s", cudaGetErrorString(e));
     so->a = a;
@@ -1177,9 +1146,6 @@ bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys,
     off += up(rows * D * 4);
     plan->off_fix_o = off;
     off += up(frows * D * 4);
-    // f32 queries on the tensor-core kernel: their f16 hi and lo terms
-    plan->off_qsplit = off;
-    off += (size_t)2 * B * Hq * D * 2;
     plan->bytes = off;
     return true;
 }

@@ -432,16 +432,14 @@ def main(argv=None):
             out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float32 if o32 else torch.float16,
                               device=dev)
             runs[n] = (lambda c=c, ws=ws, out=out: attn.decode(c, out=out, workspace=ws))
-            # f32 queries on the tensor-core kernel add the hi/lo split launch
-            extra = 1 if (c.q.dtype == torch.float32 and not c.int8 and c.head_dim != 256) else 0
-            work[n] = ("GB/s", decode_bytes(c, 4 if o32 else 2), "hbm", 2 + extra)
+            work[n] = ("GB/s", decode_bytes(c, 4 if o32 else 2), "hbm", 2)
         elif si.WORKLOADS[n]["kind"] == "tiered":
             ws = torch.empty(attn.attn_decode_tiered_workspace_size(c.batch, c.n_heads, c.n_kv_heads, c.head_dim,
                                                                     c.cap, c.hot_ring), dtype=torch.uint8,
                              device=dev)
             out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float16, device=dev)
             runs[n] = (lambda c=c, ws=ws, out=out: attn.decode_tiered(c, out=out, workspace=ws))
-            work[n] = ("GB/s", tiered_bytes(c), "hbm", 3 + (1 if c.q.dtype == torch.float32 else 0))
+            work[n] = ("GB/s", tiered_bytes(c), "hbm", 3)
         elif si.WORKLOADS[n]["kind"] == "chunked":
             out = torch.empty_like(c.q)
             runs[n] = (lambda c=c, out=out: attn.prefill_paged(c, out=out))
