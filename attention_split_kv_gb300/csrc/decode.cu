@@ -99,6 +99,7 @@ struct DecArgs {
     int B, Hq, Hkv, G, HG, U, n_hb, nh_box, split, cap_eff, window, P, R, max_pages, n_pages, paged;
     int ring;          // > 0: contiguous ring cache, logical token t in row t % ring
     int logR;          // log2(R): rows per box are a power of two (a tile or a page)
+    int logP;          // log2(P) (paged)
     // tiered decode: kTierCold reads kv_len = cold lengths (window counted from the
     // newest hot token), kTierHot the hot ring (hot_len, hot_start); kTierPlain alone
     int tier;
@@ -862,6 +863,8 @@ DecArgs make_dec_args(const DecodeLaunch& L, const DecodePlan& plan, int R) {
     a.R = R;
     a.logR = 0;
     while ((1 << a.logR) < R) ++a.logR;
+    a.logP = 0;
+    while (paged && (1 << a.logP) < L.page_size) ++a.logP;
     a.max_pages = L.max_pages;
     a.n_pages = paged ? L.n_pages : 0;
     a.paged = paged;
@@ -947,19 +950,22 @@ int decode_grid(const DecodePlan& plan) {
     return grid < 1 ? 1 : (int)grid;
 }
 
-// Tensor-core split kernel: f16 caches, head_dim 64/128, boxes of 16 rows x NH heads.
-// Q2: f32 queries (split into f16 hi and lo terms by the kernel as it loads them).
+// Tensor-core split kernel: f16 caches with head_dim 64/128; boxes of R rows x
+// NH heads.  Q2: f32 queries (split into f16 hi and lo terms by the kernel as it
+// loads them).
 template <int D, int NH, bool Q2>
 attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, SplitOut* so) {
     using C = tcdec::Cfg<D, Q2>;
     const bool paged = L.page_table != nullptr;
+    // rows per box: 16, or the page size when pages are shorter (R * NH >= 8)
+    const int R = paged && L.page_size < 16 ? L.page_size : 16;
     CUtensorMap tk, tv;
     attn_status st;
     const int q_rows = L.Hq < tcdec::QROWS ? L.Hq : tcdec::QROWS;
     {
-        // [pages or B][rows][Hkv][D]: boxes of (64 dims, NH heads, 16 rows, 1), 128-byte swizzle
+        // [pages or B][rows][Hkv][D]: boxes of (64 dims, NH heads, R rows, 1), 128-byte swizzle
         uint64_t dims[4], strides[3];
-        const uint32_t box[4] = {64u, (uint32_t)NH, 16u, 1u};
+        const uint32_t box[4] = {64u, (uint32_t)NH, (uint32_t)R, 1u};
         dims[0] = D;
         dims[1] = L.Hkv;
         dims[2] = paged ? L.page_size : L.max_kv;
@@ -981,7 +987,7 @@ attn_status launch_decode_tc(const DecodeLaunch& L, const DecodePlan& plan, Spli
             return set_error(ATTN_ECUDA, "cudaFuncSetAttribute(decode tc smem) failed");
         attr_set[dev] = true;
     }
-    const DecArgs a = make_dec_args(L, plan, 16);
+    const DecArgs a = make_dec_args(L, plan, R);
     // balanced: every CTA takes an equal share of the tiles (see decode_tc.cuh)
     const int grid = sm_count() < plan.n_fix ? sm_count() : plan.n_fix;
     if (trace_enabled())
@@ -1006,12 +1012,14 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan, Split
     const CUtensorMapDataType kvt = I8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const bool paged = L.page_table != nullptr;
     if constexpr (!I8 && D != 256) {
-        // both contractions on the tensor cores where the boxes allow it:
-        // 16-row boxes must not cross a page, and cover at most Hkv heads;
-        // batches of up to 2048 sequences
+        // both contractions on the tensor cores where the boxes allow it: a
+        // box covers at most Hkv heads and 16 rows of one page; with pages
+        // shorter than 16 tokens each box of P rows must start 1024-byte aligned
+        // (P * NH >= 8); batches of up to 2048
         int nh = 1;
         while (nh < plan.nh_box) nh <<= 1;
-        if ((!paged || L.page_size % 16 == 0) && nh <= L.Hkv && L.B <= tcdec::kMaxBatch) {
+        const bool boxes_ok = !paged || L.page_size % 16 == 0 || L.page_size * nh >= 8;
+        if (boxes_ok && nh <= L.Hkv && L.B <= tcdec::kMaxBatch) {
             switch (nh) {
                 case 1: return L.q_f32 ? launch_decode_tc<D, 1, true>(L, plan, so) : launch_decode_tc<D, 1, false>(L, plan, so);
                 case 2: return L.q_f32 ? launch_decode_tc<D, 2, true>(L, plan, so) : launch_decode_tc<D, 2, false>(L, plan, so);

@@ -183,10 +183,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                  const int q_rows) {
     using C = Cfg<D, Q2>;
     constexpr int NCH = C::NCH, NK = C::NK, NV = C::NV, NOB = C::NOB;
-    constexpr int NBX = 8 / NH;                 // 16-token boxes per MMA tile
     constexpr int TT = TR / NH;                 // tokens per MMA tile
     constexpr int TQ = TT / kSoftmaxWarps;      // tokens of a tile in one quadrant
-    constexpr uint32_t BOXB = 16 * NH * 128;    // bytes of one box (one chunk)
     constexpr int NXC = D / 32;                 // 32-column chunks of O merged per run
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -269,24 +267,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 }
                 const int g0 = (c.hb * NW) / A.HG;
                 const int t0 = c.a + c.t * TT;
-                const int nbox = min(NBX, (c.end - t0 + 15) / 16);
-                mbar_arrive_expect_tx(bar(b_full + slot), nbox * NCH * BOXB);
+                // boxes of R rows (16, or the page size when pages are shorter, with
+                // R * NH >= 8 so that every box starts 1024-byte aligned, as the
+                // 128-byte swizzle requires); boxes wholly past the end are skipped
+                const int R = A.R;
+                const int nbox = (min(TT, c.end - t0) + R - 1) / R;
+                mbar_arrive_expect_tx(bar(b_full + slot), nbox * NCH * R * NH * 128);
                 for (int bx = 0; bx < nbox; ++bx) {
-                    const int tk = t0 + bx * 16;
+                    const int tk = t0 + bx * R;
                     int page = c.b, row = A.ring > 0 ? tk % A.ring : tk;   // ring: slot t % ring (ring % 16 == 0)
                     if (A.paged) {
-                        page = __ldg(&A.page_table[(size_t)c.b * A.max_pages + tk / A.P]);
+                        page = __ldg(&A.page_table[(size_t)c.b * A.max_pages + (tk >> A.logP)]);
                         if (page < 0 || page >= A.n_pages) {
                             // a page id outside the pool: read page 0 instead and report it
                             atomicExch(A.err, kErrBadPage);
                             page = 0;
                         }
-                        row = tk % A.P;
+                        row = tk & (A.P - 1);
                     }
 #pragma unroll
                     for (int ch = 0; ch < NCH; ++ch)
-                        tma_load_4d(ring + slot * C::KV_BYTES + ch * C::CHUNK + bx * BOXB, tm, bar(b_full + slot),
-                                    ch * 64, g0, row, page);
+                        tma_load_4d(ring + slot * C::KV_BYTES + ch * C::CHUNK + bx * R * NH * 128, tm,
+                                    bar(b_full + slot), ch * 64, g0, row, page);
                 }
             }
             if (!ok) {
@@ -460,6 +462,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             A.ws_fix_meta[blockIdx.x] = tag;
         }
         if (c.x < c.x_end) q_row(c.b, c.hb);       // the first run's Q'
+        bool ok = true;
 
         // a run's epilogue, run one tile late: the four quadrant partials of this
         // thread's query head merged by log-sum-exp (weights 2^(m_w - M) in a fixed
@@ -558,11 +561,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         };
 
         uint32_t j = 0;
-        bool ok = true;
         bool act = false;
         int gl = 0, t_first = 0;
         float m_used = -INFINITY, l_sum = 0.f;
-        for (; c.x < c.x_end; tcur_next<TT>(c, tpref, A), ++j) {
+        for (; ok && c.x < c.x_end; tcur_next<TT>(c, tpref, A), ++j) {
             if (c.first) {
                 const int u = c.hb * NW + wu;
                 act = wu < NW && r < QB && u < A.U;
@@ -601,6 +603,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 next_run(c, nb, nhb);
                 if (nb >= 0) q_row(nb, nhb);
             }
+
             // this quadrant's tokens of the tile: tok0 .. tok0 + TQ - 1
             const int t0 = c.a + c.t * TT;
             const int tok0 = qd * TQ;

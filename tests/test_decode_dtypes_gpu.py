@@ -1,7 +1,8 @@
 """GPU parity of the decode query and output element types (attn_decode_ex,
 attn_decode_tiered): f32 queries on the tensor-core kernel (two f16 terms into
-one accumulator) and on the CUDA-core kernel (read as f32), f32 outputs, and the
-bit-identities that tie them to the f16 path."""
+one accumulator) and on the CUDA-core kernel (read as f32, or 16-bit fixed
+point for int8 caches), f32 outputs, and the bit-identities that tie them to
+the f16 path."""
 import numpy as np
 import pytest
 import torch
@@ -39,7 +40,8 @@ CASES = {
     "tc_d128_ring": (128, False, 0, 64),
     "cc_d256": (256, False, 0, 0),
     "cc_int8_paged": (128, True, 16, 0),
-    "cc_paged8": (128, False, 8, 0),
+    "cc_int8_contig": (128, True, 0, 0),
+    "cc_paged2": (128, False, 2, 0),
 }
 
 

@@ -68,21 +68,52 @@ def test_decode_paged(page_size, int8):
 
 
 @pytest.mark.parametrize("int8", [False, True], ids=["f16", "int8"])
-@pytest.mark.parametrize("page_size", [8, 16, 32])
+@pytest.mark.parametrize("page_size", [1, 2, 4, 8, 16, 32])
 def test_paged_is_bit_identical_to_contiguous(page_size, int8):
-    # the page table only changes where rows are read from: the same kernel
-    # gives the same bits.  f16 caches with pages of a multiple of 16 tokens run
-    # the tensor-core kernel like the contiguous cache; pages of 8 f16 tokens run
-    # the CUDA-core kernel, which rounds differently, so there the two agree to
-    # the parity tolerance instead.
+    # the page table only changes where rows are read from: both layouts run the
+    # same kernel and give the same bits.  int8 caches run the CUDA-core kernel
+    # for every layout.  Here (8 query / 2 kv heads, D=128) an f16 TMA box spans
+    # NH=2 kv heads; the tensor-core kernel takes pages of 16k tokens, and pages
+    # of P tokens with P * NH >= 8 (P >= 4), each box of P rows starting
+    # 1024-byte aligned.  Shorter f16 pages run the CUDA-core kernel while the
+    # contiguous cache runs the tensor-core one: there the two agree to the
+    # parity tolerance; the tests below pin bit-identity for those page sizes
+    # where one kernel runs both.
+    if int8 and page_size < 8:
+        pytest.skip("int8 caches need pages of >= 8 tokens")
     case = si.make_decode_case(3, 8, 2, 128, [5, 450, 300], seed=41, int8=int8, cap=456)
     paged = si.paged_from_contiguous(case, page_size, seed=42)
     a, la = _run(case, split_keys=64, max_kv=456)
     b, lb = _run(paged, split_keys=64, max_kv=456)
-    if int8 or page_size % 16 == 0:
+    same_kernel = int8 or page_size % 16 == 0 or page_size * 2 >= 8
+    if same_kernel:
         assert np.array_equal(a, b) and np.array_equal(la, lb)
     else:
         assert np.abs(a - b).max() <= 2e-3 and np.abs(la - lb).max() <= 1e-3
+
+
+@pytest.mark.parametrize("page_size", [1, 2, 8])
+def test_one_token_pages_bit_identical_on_the_tensor_core_kernel(page_size):
+    # 32 query / 8 kv heads: a box spans NH=8 kv heads, so even 1-token pages
+    # start every box 1024-byte aligned and run the tensor-core kernel
+    case = si.make_decode_case(3, 32, 8, 128, [5, 450, 300], seed=43, cap=456)
+    paged = si.paged_from_contiguous(case, page_size, seed=44)
+    a, la = _run(case, split_keys=64, max_kv=456)
+    b, lb = _run(paged, split_keys=64, max_kv=456)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["f16", "int8"])
+@pytest.mark.parametrize("page_size", [1, 8, 16])
+def test_paged_bit_identical_on_the_cuda_core_kernel(page_size, int8):
+    # D=256 runs the CUDA-core kernel for both layouts, whatever the page size
+    if int8 and page_size < 8:
+        pytest.skip("int8 caches need pages of >= 8 tokens")
+    case = si.make_decode_case(3, 8, 2, 256, [5, 450, 300], seed=45, int8=int8, cap=456)
+    paged = si.paged_from_contiguous(case, page_size, seed=46)
+    a, la = _run(case, split_keys=64, max_kv=456)
+    b, lb = _run(paged, split_keys=64, max_kv=456)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
 
 
 @pytest.mark.parametrize("window", [1, 5, 16, 100, 5000])

@@ -56,10 +56,13 @@ def test_prefill_timeout_reports_and_recovers(D):
     assert_close(out.float().cpu().numpy().reshape(ref.shape), ref, what="after timeout D=%d" % D)
 
 
-@pytest.mark.parametrize("kind", ["tensor_core_f16", "cuda_core_int8"])
+@pytest.mark.parametrize("kind", ["tensor_core_f16", "cuda_core_int8", "cuda_core_d256"])
 def test_decode_timeout_reports_and_recovers(kind):
+    # f16 with D=128 and 16-token pages runs the tensor-core kernel; int8 caches
+    # and D=256 run the CUDA-core kernel
     int8 = kind == "cuda_core_int8"
-    case = si.make_decode_case(3, 8, 2, 128, [700, 33, 1000], seed=11, int8=int8, page_size=16)
+    D = 256 if kind == "cuda_core_d256" else 128
+    case = si.make_decode_case(3, 8, 2, D, [700, 33, 1000], seed=11, int8=int8, page_size=16)
     g = case.to("cuda")
     assert _stalled(lambda: attn.decode(g)) == attn.ATTN_ETIMEOUT
     ref, _ = oracle.decode(case)
