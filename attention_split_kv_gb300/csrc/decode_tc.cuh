@@ -316,6 +316,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const bool stall = stall_first_tile();
             const uint64_t limit = *static_cast<volatile unsigned long long*>(&g_wait_limit_ns);
             uint64_t t_idle = globaltimer();
+            // base descriptors, built once: each MMA's operand is a constant offset
+            // from them (this thread shares its issue slots with a softmax warp)
+            const uint64_t k_desc = smem_desc_sw128(sbase + C::OFF_RING, 16, 1024);
+            const uint64_t v_desc = smem_desc_sw128(sbase + C::OFF_VRING, C::CHUNK, 1024);
             for (uint32_t spin = 0; cs.x < cs.x_end || cp.x < cp.x_end; ++spin) {
                 bool progress = false;
                 if (cs.x < cs.x_end) {
@@ -324,10 +328,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                         (js == 0 || mbar_test_wait(bar(B_SFREE), (js - 1) & 1)) &&
                         mbar_test_wait(bar(B_KFULL + slot), (js / NK) & 1)) {
                         tc_fence_after();
-                        const uint32_t kb = sbase + C::OFF_RING + slot * C::KV_BYTES;
+                        const uint64_t kd = desc_advance(k_desc, slot * C::KV_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t b = smem_desc_sw128(kb + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024);
+                            const uint64_t b = desc_advance(kd, (kk >> 2) * C::CHUNK + (kk & 3) * 32);
                             tc_mma_f16_ts(tmem + C::COL_S, tmem + C::COL_Q + kk * 8, b, idesc_s, kk != 0);
                             if constexpr (Q2)
                                 tc_mma_f16_ts(tmem + C::COL_S, tmem + C::COL_Q + D / 2 + kk * 8, b, idesc_s, 1u);
@@ -346,11 +350,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                         (!cp.first || cp.run < NOB || mbar_test_wait(bar(B_OFREE + ob), ((cp.run / NOB) - 1) & 1)) &&
                         mbar_test_wait(bar(B_VFULL + slot), (jp / NV) & 1)) {
                         tc_fence_after();
-                        const uint32_t vb = sbase + C::OFF_VRING + slot * C::KV_BYTES;
+                        const uint64_t vd = desc_advance(v_desc, slot * C::KV_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < TR / 16; ++kk) {
                             // 16 rows per MMA: 8 TMEM columns of P, 16 rows of V (2048 bytes)
-                            const uint64_t b = smem_desc_sw128(vb + kk * 16 * 128, C::CHUNK, 1024);
+                            const uint64_t b = desc_advance(vd, kk * 16 * 128);
                             tc_mma_f16_ts(tmem + C::COL_O + ob * D, tmem + C::COL_P + kk * 8, b, idesc_o,
                                           (!cp.first || kk > 0) ? 1u : 0u);
                         }

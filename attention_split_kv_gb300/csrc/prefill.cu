@@ -382,16 +382,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 // testing hook: hold back the signal of the first S tile, so that the
                 // softmax's wait for it runs out (the failure path, without a fault)
                 const bool stall = stall_first_tile();
+                // base descriptors, built once: each MMA's operands are a constant
+                // offset from them (this thread shares its issue slots with softmax warps)
+                const uint64_t q_desc = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
+                const uint64_t k_desc = smem_desc_sw128(sbase + C::OFF_K, 16, 1024);
+                const uint64_t v_desc = smem_desc_sw128(sbase + C::OFF_V, C::KV_CHUNK, 1024);
                 auto issue_s = [&](int j) {
                     const int st = j % C::KST;
                     const uint32_t d_tmem = tmem + (j % NBUF) * BN;
+                    const uint64_t kd = desc_advance(k_desc, st * C::KV_BYTES);
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = smem_desc_sw128(sbase + C::OFF_Q + c * (BM * 128) + kk * 32, 16, 1024);
-                            const uint64_t b = smem_desc_sw128(
-                                sbase + C::OFF_K + st * C::KV_BYTES + c * C::KV_CHUNK + kk * 32, 16, 1024);
+                            const uint64_t a = desc_advance(q_desc, c * (BM * 128) + kk * 32);
+                            const uint64_t b = desc_advance(kd, c * C::KV_CHUNK + kk * 32);
                             tc_mma_f16_ss(d_tmem, a, b, idesc_s, (c | kk) != 0);
                         }
                     }
@@ -420,12 +425,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (!mbar_wait(bar(B_VFULL + st), (j / C::VST) & 1, abort_flag, args.err, kErrTimeoutLoad)) break;
                     tc_fence_after();
                     const uint32_t p_tmem = tmem + C::COL_P + (j % NBUF) * C::P_COLS;
-                    const uint32_t v_base = sbase + C::OFF_V + st * C::KV_BYTES;
+                    const uint64_t vd = desc_advance(v_desc, st * C::KV_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
                         // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V (2048 bytes)
-                        const uint64_t b = smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
-                        tc_mma_f16_ts(tmem + C::COL_O, p_tmem + kk * 8, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_f16_ts(tmem + C::COL_O, p_tmem + kk * 8, desc_advance(vd, kk * 16 * 128), idesc_o,
+                                      (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(bar(B_PVDONE + (j % NBUF)));
                     tc_commit(bar(B_VEMPTY + st));

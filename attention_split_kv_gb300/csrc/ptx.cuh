@@ -275,6 +275,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// The descriptor of an operand `bytes` further on: the start address field is
+// addr >> 4 in the low 14 bits, and every shared-memory address of these
+// kernels stays below 256 KB, so it is a plain add (no carry out of the field).
+// Lets the MMA issuer build one base descriptor per buffer instead of one per MMA.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+    return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 with f16 A/B and f32 accumulation:
 //   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16), 10-12 B format,
 //   bit 15 A major (0 = K-major), bit 16 B major (1 = MN-major),

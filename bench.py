@@ -484,7 +484,8 @@ def main(argv=None):
         one_step(evs[k])
     torch.cuda.synchronize()
     barrier(world)
-    ms = {n: sum(evs[k][n][0].elapsed_time(evs[k][n][1]) for k in range(args.steps)) / args.steps for n in names}
+    per_call = {n: sorted(evs[k][n][0].elapsed_time(evs[k][n][1]) for k in range(args.steps)) for n in names}
+    ms = {n: sum(v) / len(v) for n, v in per_call.items()}
     status = attn.attn_device_status()
     # ---- e2e: headline through the same call with host buffers and copies timed.
     # Pipelined over steps the way a serving loop runs: two sets of device
@@ -570,6 +571,8 @@ def main(argv=None):
         per_gpu = amount / (ms[n] * 1e-3) / div
         peak = peaks[key]
         results[n] = {"value": value, "unit": unit, "ms": t_ms, "launches_per_call": launches,
+                      "us_min_median_max": [round(1000 * per_call[n][0], 2), round(1000 * per_call[n][len(per_call[n]) // 2], 2),
+                                            round(1000 * per_call[n][-1], 2)],
                       "roofline": {"bound": bound, "achieved": per_gpu, "peak": peak,
                                    "unit": unit, "frac": per_gpu / peak, "traffic": NCU_TRAFFIC.get(n),
                                    "peak_source": peaks["source"],
