@@ -30,7 +30,6 @@ __device__ int g_validate_seq = 0x7fffffff;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int* g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -102,16 +101,13 @@ void trace(const char* fmt, ...) {
     std::fprintf(stderr, "[libattn] %s\n", line);
 }
 
+// Looked up on every call rather than cached: after cudaDeviceReset (or any
+// teardown and re-creation of the context) the module reloads at another
+// address.  Once the module is loaded the lookup is a host-side table read.
 int* device_error_word() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_err_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-        g_err_ptr[dev] = static_cast<int*>(p);
-    }
-    return g_err_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    return static_cast<int*>(p);
 }
 
 int sm_count() {

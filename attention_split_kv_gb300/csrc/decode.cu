@@ -1205,10 +1205,12 @@ attn_status set_test_controls_decode(unsigned long long wait_limit_ns, int stall
 // process exits.
 //
 // The array's name means nothing to host code (it is a host-side shadow, not
-// a device address), so the device address is looked up once per device with
-// cudaGetSymbolAddress while that device is current, and passed to the
-// kernels like any workspace pointer.  That lookup happens inside the first
-// call on each device; make that first call before any stream capture.
+// a device address), so every call looks the device address up with
+// cudaGetSymbolAddress on the current device and passes it to the kernels
+// like any workspace pointer.  The lookup is not cached: after cudaDeviceReset
+// the module reloads at another address.  The first call on a device loads
+// the module (lazy loading), which reserves the array; make that first call
+// at initialisation, before any stream capture or latency-critical loop.
 // Nothing in the scratch needs to start at zero: every byte the kernels read
 // is written earlier in the same call.  All calls share the one array, so two
 // calls whose kernels overlap on the GPU (different streams, no ordering)
@@ -1222,25 +1224,13 @@ static __device__ __align__(256) unsigned char g_decode_scratch[attn::kNoAllocSc
 
 namespace attn {
 namespace {
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {};
-
-// Device address of g_decode_scratch on the current device (looked up once).
+// Device address of g_decode_scratch on the current device.
 attn_status scratch_for_current_device(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return set_error(ATTN_ECUDA, "attn_decode_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= 64) return set_error(ATTN_EUNSUPPORTED, "attn_decode_noalloc: device index %d above 63", dev);
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess || p == nullptr)
-            return set_error(ATTN_ECUDA, "attn_decode_noalloc: cudaGetSymbolAddress(scratch): %s",
-                             cudaGetErrorString(e));
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess || p == nullptr)
+        return set_error(ATTN_ECUDA, "attn_decode_noalloc: cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    *out = p;
     return ATTN_OK;
 }
 }  // namespace

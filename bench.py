@@ -56,11 +56,12 @@ HEADLINE = "vision_2304"
 NCU_TRAFFIC = {
     "vision_2304": 14.24e6,
     "swa_softcap_prefill": 33.63e6,
-    "paged_gqa_decode": 583.3e6,
+    "paged_gqa_decode": 583.6e6,
     "int8_long_decode": (136.54e6 + 8.53e6) * 8,
     "chunked_prefill_paged": 236.18e6,
-    "ring_window_decode": 543.1e6,
-    "paged_decode_f32io": 593.2e6,
+    "ring_window_decode": None,      # kernel changed since its capture
+    "tiered_int8_decode": 652.8e6,   # cold split + hot split + combine, one call
+    "paged_decode_f32io": None,      # kernel changed since its capture
 }
 METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
 WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode",

@@ -263,10 +263,14 @@ attn_status attn_decode_tiered(const void* q, attn_dtype q_dtype,
  * compiled into the library; every GPU that loads the library holds that
  * array until the process exits.  Sizes whose attn_decode_workspace_size
  * exceeds 16 MiB are rejected with ATTN_EUNSUPPORTED (a larger split_keys
- * lowers the need).  Nothing is allocated and no allocating routine is
- * called.  The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array and no part of it
+ * lowers the need).  The calls themselves allocate nothing, but the array is
+ * reserved when the library's device module loads: at context creation with
+ * eager module loading, else (lazy loading, the default) inside the first
+ * call of the library on that device, which may synchronise the device.
+ * Make one warm-up call at initialisation, outside stream capture and
+ * latency-critical loops.  Every call looks the array's device address up
+ * (cudaGetSymbolAddress, no allocation once loaded), so a cudaDeviceReset
+ * between calls is safe.  All calls share the one array and no part of it
  * needs to start at zero; calls whose kernels overlap on the GPU (different
  * streams without ordering) race on it, so order them on one stream.
  */
