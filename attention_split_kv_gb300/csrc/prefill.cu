@@ -172,7 +172,8 @@ constexpr int kLptMaxPairs = 128;
 template <int D, int MODE, bool PAGED>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, PrefillCfg<D>::CTAS_PER_SM)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const PrefillArgs args) {
     using C = PrefillCfg<D>;
     constexpr int BN = C::BN, NCH = C::NCH, STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -217,27 +218,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         };
         if (args.lpt) {
             // longest first across sequences: CTA x takes head x % Hq of the
-            // (x / Hq)-th (sequence, query tile) pair in decreasing order of key
-            // tiles (ties by index), so the last wave holds the shortest CTAs.
-            // The scratch sits where Q lands, before any copy is issued.
+            // (x / Hq)-th (sequence, query tile) pair, pairs ranked by the key
+            // tiles of their sequence's longest query tile, then by their own
+            // (ties by index).  The last wave holds the shortest CTAs, and the
+            // query tiles of one sequence (which read the same pages) run next
+            // to each other, so those pages come from DRAM about once.  The
+            // scratch sits where Q lands, before any copy is issued.
             int* wk = reinterpret_cast<int*>(smem + C::OFF_Q);
-            int* sel = wk + kLptMaxPairs;
+            int* wseq = wk + kLptMaxPairs;
+            int* sel = wseq + kLptMaxPairs;
             const int n_pairs = args.B * args.max_qt;
             if (threadIdx.x < n_pairs) {
                 const int bb = threadIdx.x / args.max_qt, t = threadIdx.x % args.max_qt;
-                int qs, nq, Lb, p0, j0, w = -1;   // -1: no queries, ranked last
+                int qs, nq, Lb, p0, j0, w = -1, ws = -1;   // -1: no queries, ranked last
                 chunk_of(bb, qs, nq, Lb, p0);
-                if (t * BM < nq) w = key_tiles(Lb, p0, t * BM, min(t * BM + BM - 1, nq - 1), j0);
+                if (t * BM < nq) {
+                    w = key_tiles(Lb, p0, t * BM, min(t * BM + BM - 1, nq - 1), j0);
+                    const int tl = (nq - 1) / BM;
+                    ws = key_tiles(Lb, p0, tl * BM, nq - 1, j0);
+                }
                 wk[threadIdx.x] = w;
+                wseq[threadIdx.x] = ws;
             }
             __syncthreads();
             const int want = static_cast<int>(blockIdx.x) / args.Hq;
             if (threadIdx.x < n_pairs) {
-                const int me = wk[threadIdx.x];
+                const int me = wk[threadIdx.x], ms = wseq[threadIdx.x];
                 int rank = 0;
                 for (int j = 0; j < n_pairs; ++j) {
-                    const int o = wk[j];
-                    rank += (o > me || (o == me && j < static_cast<int>(threadIdx.x))) ? 1 : 0;
+                    const int o = wk[j], os = wseq[j];
+                    rank += (os > ms || (os == ms && (o > me || (o == me && j < static_cast<int>(threadIdx.x))))) ? 1
+                                                                                                                : 0;
                 }
                 if (rank == want) *sel = threadIdx.x;   // ranks are a permutation: one writer
             }
@@ -672,6 +683,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (ok) ok = exchange(l_sum, 4, n_tiles, other);
             l_sum += other;
         }
+        // D=256: whole tiles leave through shared memory and tiled bulk stores (rows past
+        // S are clipped by the tensor map).  Row by row, each thread's 256 bytes per
+        // 128 columns would go out as 16-byte pieces 4 KB apart, one L2 sector per lane
+        // and store; D=64/128 have a quarter or half of that and keep the direct stores,
+        // which let the CTA retire without waiting for a bulk copy.  A chunk's last,
+        // partial tile is stored row by row, since the rows after it belong to the next
+        // sequence.  The staging area is Q's: every MMA has retired.
+        bool via_tma = D == 256;
+        if constexpr (PAGED) via_tma = via_tma && q0 + BM <= n_q && q_base >= 0 && q_base + q0 + BM <= args.total_q;
+        uint8_t* stage = smem + C::OFF_Q;
         if (ok) {
             tc_fence_after();
             const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
@@ -691,13 +712,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = 0.f;   // no key at all: O was never written
                 }
-                if (row_ok) {
-                    uint32_t hv[16];
+                uint32_t hv[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const __half2 p2 = __floats2half2_rn(o[2 * i], o[2 * i + 1]);
-                        hv[i] = *reinterpret_cast<const uint32_t*>(&p2);
-                    }
+                for (int i = 0; i < 16; ++i) {
+                    const __half2 p2 = __floats2half2_rn(o[2 * i], o[2 * i + 1]);
+                    hv[i] = *reinterpret_cast<const uint32_t*>(&p2);
+                }
+                if (via_tma) {
+                    // columns col0 .. col0+31 of this row: 16-byte units u0 .. u0+3 of its
+                    // 128-byte line in chunk col0 / 64, at the 128-byte swizzle's positions
+                    const int col0 = ch * OW + c * 32;
+                    uint8_t* line = stage + (col0 >> 6) * (BM * 128) + row * 128;
+                    const int u0 = (col0 & 63) >> 3;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<uint4*>(line + (((u0 + i) ^ (row & 7)) << 4)) =
+                            make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+                } else if (row_ok) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + ch * OW + c * 32);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
@@ -706,6 +737,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (args.lse && row_ok && ch == 0) {
                 args.lse[static_cast<size_t>(q_base + qi) * args.Hq + h] =
                     l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
+            }
+        }
+        if (via_tma) {
+            // every softmax thread's staged lines are visible to the bulk copy, then
+            // one thread stores the tile and waits until its reads of shared memory are done
+            fence_proxy_async_smem();
+            named_bar_sync(1, C::NSM * 32);
+            if (threadIdx.x == 0 && ok) {
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) tma_store_3d(&tm_o, smem_u32(stage + c * (BM * 128)), c * 64, h, q_base + q0);
+                tma_store_commit();
+                tma_store_wait_read();
             }
         }
     }
@@ -720,18 +763,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 template <int D, int MODE, bool PAGED>
 attn_status launch_prefill_dm(const PrefillLaunch& L) {
     using C = PrefillCfg<D>;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     attn_status st;
     int box_rows = C::BN;
     if (!PAGED) {
         // 3-D maps over [S, H, D] f16: dims (D, H, S), 64-element x rows boxes, 128-byte swizzle
         if ((st = encode_tmap_3d_f16_sw128(&tq, L.q, D, L.Hq, L.S, BM)) != ATTN_OK) return st;
+        if ((st = encode_tmap_3d_f16_sw128(&to, L.out, D, L.Hq, L.S, BM)) != ATTN_OK) return st;
         if ((st = encode_tmap_3d_f16_sw128(&tk, L.k, D, L.Hkv, L.S, C::BN)) != ATTN_OK) return st;
         if ((st = encode_tmap_3d_f16_sw128(&tv, L.v, D, L.Hkv, L.S, C::BN)) != ATTN_OK) return st;
     } else {
         // q [total_q, Hq, D] as above; the pool [n_pages, P, Hkv, D] as (D, Hkv, P, n_pages)
         // with boxes of (64, 1 head, min(P, tile keys) rows, 1 page)
         if ((st = encode_tmap_3d_f16_sw128(&tq, L.q, D, L.Hq, L.total_q, BM)) != ATTN_OK) return st;
+        if ((st = encode_tmap_3d_f16_sw128(&to, L.out, D, L.Hq, L.total_q, BM)) != ATTN_OK) return st;
         box_rows = L.page_size < C::BN ? L.page_size : C::BN;
         const uint64_t dims[4] = {(uint64_t)D, (uint64_t)L.Hkv, (uint64_t)L.page_size, (uint64_t)L.n_pages};
         const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)D * 2 * L.Hkv,
@@ -785,9 +830,9 @@ attn_status launch_prefill_dm(const PrefillLaunch& L) {
               D, MODE == kModeRaw ? "raw" : MODE == kModeScaled ? "scaled" : "capped", (int)PAGED, grid.x, grid.y,
               grid.z, C::THREADS, C::SMEM_ALLOC, C::TMEM_COLS, C::CTAS_PER_SM, C::BN, PAGED ? L.total_q : L.S,
               L.Hq, L.Hkv, L.causal, L.window, L.softcap, L.scale,
-              PAGED ? (a.lpt ? " order=longest-first" : " order=(tile,head,seq)")
+              PAGED ? (a.lpt ? " order=heads fastest, sequences longest first, their query tiles together" : " order=(tile,head,seq)")
                     : L.causal ? " order=heads fastest, longest query tiles first" : " order=heads fastest");
-    prefill_tc_kernel<D, MODE, PAGED><<<grid, C::THREADS, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, a);
+    prefill_tc_kernel<D, MODE, PAGED><<<grid, C::THREADS, C::SMEM_ALLOC, L.stream>>>(tq, tk, tv, to, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
