@@ -11,16 +11,18 @@
 // each sequence is cut into fixed-size splits so the whole GPU streams the
 // cache:
 //
-//   decode_split_kernel   persistent, one CTA of 8 warps per SM.  A work item
+//   decode_split_kernel   persistent, one CTA per SM: 8 consumer warps (and,
+//                         for int8, a producer warp).  A work item
 //                         is (sequence, head block, split): a head block is up
 //                         to 8 (kv head, query-head group) units and warp w
 //                         owns unit w for the whole split.  Tiles of 16 tokens
 //                         (8 for D=256) of every kv head of the block are one
 //                         TMA box per tensor (per page when paged): tens of KB
 //                         contiguous in the cache, so a handful of copies keep
-//                         HBM busy.  Warp 0's lane 0 also issues those copies,
-//                         NSLOT-1 tiles ahead, into a ring of shared-memory
-//                         slots with full/empty mbarriers.  Inside a warp,
+//                         HBM busy.  The producer warp (f16: warp 0's lane 0,
+//                         between its own tiles) issues those copies ahead
+//                         into a ring of shared-memory slots (full/empty
+//                         mbarriers).  Inside a warp,
 //                         8 (16 for D=256) lanes share one key: each lane
 //                         holds D/8 dims of the GH query heads of its unit in
 //                         registers, so a K row is read once for GH heads
@@ -43,14 +45,19 @@
 namespace attn {
 namespace {
 
-constexpr int NW = 8;                     // warps per CTA = units per head block
-constexpr int kDecThreads = NW * 32;
+constexpr int NW = 8;                     // consumer warps per CTA = units per head block
 constexpr int kSmemBudget = 226 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D, bool I8, int GH>
 struct DecCfg {
+    // int8: a ninth warp issues the copies, so that no consumer interleaves them
+    // with its own tiles (9 warps are allocated registers as 12: 168 a thread).
+    // f16 (more registers a lane) keeps the copies on consumer warp 0.
+    static constexpr int NPROD = I8 ? 1 : 0;
+    static constexpr int THREADS = (NW + NPROD) * 32;
+    static constexpr int PROD = NPROD ? NW : 0;          // the warp that issues the copies
     static constexpr int ESZ = I8 ? 1 : 2;
     static constexpr int RB = D * ESZ;                       // bytes of one K/V row
     static constexpr int LPK = (D == 256) ? 16 : 8;          // lanes sharing one key
@@ -270,7 +277,7 @@ __device__ __forceinline__ void load_row_slice(const uint8_t* row, int c, float2
 }
 
 template <int D, bool I8, int GH>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(DecCfg<D, I8, GH>::THREADS, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
                     const DecArgs A) {
@@ -309,13 +316,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
     }
 
-    // ------------------------------------------------------------------ producer state (warp 0)
+    // ------------------------------------------------------------------ producer state (warp NW)
     // Tiles are issued in the order the CTA consumes them; `issued` counts
     // them, (p_it, p_i) is the next tile to issue.
     uint32_t issued = 0;
     int p_it = blockIdx.x, p_i = 0;
     Item p_item;
-    if (warp == 0 && p_it < total) p_item = decode_item<T>(p_it, pref, A);
+    if (warp == C::PROD && p_it < total) p_item = decode_item<T>(p_it, pref, A);
     int cache_b = -1, cache_base = -1, pid = -1;
     const int NB = T / A.R;                                   // boxes per tile per tensor
     const uint32_t box_kv = A.R * A.nh_box * C::RB;           // bytes of one K (or V) box
@@ -326,7 +333,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // testing hook: issue nothing, so that the consumers' wait for the first
     // tile runs out (the failure path, without a fault)
     const bool stall = stall_first_tile();
-    // Issue tiles until `target` (a consumption count) is covered.  Whole warp 0.
+    // Issue tiles until `target` (a consumption count) is covered.  Whole producer warp.
     auto produce_until = [&](uint32_t target) {
         while (ok && !stall && issued <= target && p_it < total) {
             const int t0 = p_item.ks + p_i * T;
@@ -405,8 +412,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int k = 0; k < C::LOG_GH; ++k) cl |= ((h >> (C::LOG_GH - 1 - k)) & 1) << (C::LOG_LPK - 1 - k);
         src_lane[h] = grp | cl;
     }
+    if (C::NPROD && warp == C::PROD) {
+        // the producer warp runs ahead of the consumers by up to the whole ring,
+        // each slot reused once all NW consumer warps have released it
+        produce_until(0xffffffffu);
+    }
     uint32_t gcons = 0;
-    for (int it = blockIdx.x; it < total; it += gridDim.x) {
+    for (int it = blockIdx.x; warp < NW && it < total; it += gridDim.x) {
         const Item I = decode_item<T>(it, pref, A);
         const int u = I.hb * NW + warp;
         const bool active = u < A.U;
@@ -474,7 +486,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         float m = -INFINITY, l = 0.f;
 
         for (int i = 0; i < I.ntile; ++i, ++gcons) {
-            if (warp == 0) produce_until(gcons + NSLOT - 1);
+            if (!C::NPROD && warp == 0) produce_until(gcons + NSLOT - 1);
             const int slot = gcons % NSLOT;
             bool got = ok && mbar_wait(full_bar(slot), (gcons / NSLOT) & 1, abort_flag, A.err, kErrTimeoutLoad);
             got = __all_sync(0xffffffffu, got);   // keep the warp converged for the shuffles below
@@ -497,9 +509,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     if constexpr (I8) {
                         // exact int32 dots of the int8 codes with the fixed-point q (dp2a)
                         const uint8_t* krow = kt + (key * A.nh_box + hl) * C::RB;
-                        int acc[GH];
+                        // two accumulators per head (lo and hi halves of each word): chains of
+                        // NV * VB / 4 dependent dp2a instead of twice that
+                        int acc[GH], acc_hi[GH];
 #pragma unroll
-                        for (int s = 0; s < GH; ++s) acc[s] = 0;
+                        for (int s = 0; s < GH; ++s) acc[s] = acc_hi[s] = 0;
 #pragma unroll
                         for (int v = 0; v < C::NV; ++v) {
                             uint32_t w[C::VB / 4];
@@ -516,9 +530,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                                 for (int s = 0; s < GH; ++s) {
                                     const int j = (v * C::EV) / 2 + 2 * i;
                                     asm("dp2a.lo.s32.s32 %0, %1, %2, %0;" : "+r"(acc[s]) : "r"(qi[s][j]), "r"(w[i]));
-                                    asm("dp2a.hi.s32.s32 %0, %1, %2, %0;" : "+r"(acc[s]) : "r"(qi[s][j + 1]), "r"(w[i]));
+                                    asm("dp2a.hi.s32.s32 %0, %1, %2, %0;" : "+r"(acc_hi[s]) : "r"(qi[s][j + 1]), "r"(w[i]));
                                 }
                         }
+#pragma unroll
+                        for (int s = 0; s < GH; ++s) acc[s] += acc_hi[s];
                         // reduce-scatter: after it, slot 0 holds the full dot of head `rot`
 #pragma unroll
                         for (int k = 0; k < C::LOG_GH; ++k) {
@@ -648,7 +664,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // this CTA's partials are written: the combine pass may be scheduled (it
     // still waits for the whole grid to finish)
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
-    if (warp == 0 && !ok && lane == 0) {
+    if (warp == C::PROD && !ok && lane == 0) {
         // let copies in flight land before shared memory is released
         const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
         for (uint32_t x = first; x < issued; ++x)
@@ -1076,10 +1092,10 @@ attn_status launch_decode_t(const DecodeLaunch& L, const DecodePlan& plan, Split
         trace("decode_split_kernel<D=%d,int8=%d,GH=%d> grid=%d block=%d smem=%d B=%d Hq=%d Hkv=%d layout=%s tier=%d "
               "split=%d head_blocks=%d box_heads=%d box_rows=%d max_items=%ld ring_slots=%d "
               "(items round-robin over the CTAs)",
-              D, (int)I8, GH, decode_grid(plan), kDecThreads, C::SMEM_ALLOC, L.B, L.Hq, L.Hkv,
+              D, (int)I8, GH, decode_grid(plan), C::THREADS, C::SMEM_ALLOC, L.B, L.Hq, L.Hkv,
               paged ? "paged" : L.ring > 0 ? "ring" : "contiguous", L.tier, plan.split, plan.n_hb, plan.nh_box, R,
               plan.max_items, C::NSLOT);
-    decode_split_kernel<D, I8, GH><<<decode_grid(plan), kDecThreads, C::SMEM_ALLOC, L.stream>>>(tk, tv, tks, tvs, a);
+    decode_split_kernel<D, I8, GH><<<decode_grid(plan), C::THREADS, C::SMEM_ALLOC, L.stream>>>(tk, tv, tks, tvs, a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode split launch failed: %s", cudaGetErrorString(e));
     so->a = a;
