@@ -17,8 +17,9 @@
 //                                               V in smem as the MN-major operand)
 //
 // Roles: warps 0-3 softmax + epilogue (thread t owns query row t = TMEM lane
-// t), warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer (D=64/128 add two
-// idle warps 6-7 to complete the second warpgroup for setmaxnreg).
+// t), warp 4 TMA producer of Q and K, warp 5 TMEM allocator + MMA issuer, warp
+// 6 TMA producer of V (D=64/128 add an idle warp 7 to complete the second
+// warpgroup for setmaxnreg; D=256 has 8 softmax warps, so these are 8-10).
 // The MMA warp issues S_{j+1} before waiting for P_j, so QK^T of the next tile
 // overlaps the softmax of the current one.  O is rescaled lazily: only when a
 // row's running max grows by more than 8 (log2 units), so P <= 2^8 stays
@@ -54,10 +55,10 @@ struct PrefillCfg {
     // softmax warpgroup: 2 CTAs x 256 threads x 128 registers at launch, then
     // 128 x 200 + 128 x 56 per CTA.  D=256 (one CTA per SM) runs two softmax
     // warpgroups that split each row's keys in halves (so every SMSP has two
-    // softmax warps), then the producer and MMA warps: 10 warps.
+    // softmax warps), then the producer, MMA and V-producer warps: 11 warps.
     static constexpr int NSM = (D == 256) ? 8 : 4;       // softmax warps
-    static constexpr int THREADS = (D <= 128) ? 256 : (NSM + 2) * 32;
-    static constexpr int PROD_WARP = NSM, MMA_WARP = NSM + 1;
+    static constexpr int THREADS = (D <= 128) ? 256 : (NSM + 3) * 32;
+    static constexpr int PROD_WARP = NSM, MMA_WARP = NSM + 1, PROD_V_WARP = NSM + 2;
     static constexpr int CW = BN_OF(D) / (NSM / 4);      // S columns per softmax thread
     static constexpr int REG_SOFTMAX = 200, REG_OTHER = 56;
     static_assert(THREADS != 256 || (REG_SOFTMAX + REG_OTHER) * 128 * CTAS_PER_SM == 65536, "register split");
@@ -305,19 +306,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp >= C::NSM) {
         // (setmaxnreg is executed by all four warps of a warpgroup)
         if constexpr (C::THREADS == 256) setmaxnreg_dec<C::REG_OTHER>();
-        if (warp == C::PROD_WARP) {
-            // ------------------------------------------------------------ TMA producer
-            // Contiguous: lane 0 loads Q and the K tiles, lane 1 the V tiles.  Paged:
-            // lanes 0-15 load K and lanes 16-31 V, lane i of a group the box of the
-            // tile's i-th page (R rows; one box inside a page when pages are longer
-            // than the tile), so the boxes of a tile are issued in parallel.  A
-            // group's leader waits for the stage and posts the byte count; each
-            // group waits only for its own stages to be released.
-            const int grp_lane = PAGED ? (lane & 15) : 0;
-            if (PAGED || lane < 2) {
-                const bool is_k = PAGED ? lane < 16 : lane == 0;
+        if (warp == C::PROD_WARP || warp == C::PROD_V_WARP) {
+            // ------------------------------------------------------------ TMA producers
+            // One warp loads Q and the K tiles, another the V tiles, so that neither
+            // waits behind the other's waits.  Contiguous: lane 0 of each.  Paged:
+            // lanes 0-15 of each, lane i the box of the tile's i-th page (R rows; one
+            // box inside a page when pages are longer than the tile), so the boxes of a
+            // tile are issued in parallel; lane 0 waits for the stage and posts the
+            // byte count.
+            const int grp_lane = PAGED ? lane : 0;
+            if (PAGED ? lane < 16 : lane == 0) {
+                const bool is_k = warp == C::PROD_WARP;
                 const bool leader = grp_lane == 0;
-                const unsigned gmask = is_k ? 0x0000ffffu : 0xffff0000u;
+                const unsigned gmask = 0x0000ffffu;
                 const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
                 const uint32_t off = is_k ? C::OFF_K : C::OFF_V;
                 const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
@@ -347,7 +348,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         int ok = 1;
                         if (leader) ok = mbar_wait(bar(b_empty + st), ((j / NST) - 1) & 1, abort_flag, args.err,
                                                    kErrTimeoutSlot);
-                        if constexpr (PAGED) ok = __shfl_sync(gmask, ok, is_k ? 0 : 16);
+                        if constexpr (PAGED) ok = __shfl_sync(gmask, ok, 0);
                         if (!ok) break;
                     }
                     const int key0 = (jt0 + j) * BN;
