@@ -695,7 +695,9 @@ struct CombTiers {
 
 // One warp per (sequence, query head): log-sum-exp merge of the splits of
 // every tier (one tier for a plain decode; cold and hot for a tiered decode).
-template <int D, int NT, typename OutT>
+// RB: partial rows read per batch (all loads in flight together): 16 for the
+// CUDA-core kernel's partials (many splits per row, no fix-up slots), 8 otherwise.
+template <int D, int NT, typename OutT, int RB>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const CombTiers<NT> T, OutT* __restrict__ out, float* __restrict__ lse_out, int B, int Hq,
                       int G, int GH, int HG, int n_hb) {
@@ -775,7 +777,7 @@ decode_combine_kernel(const CombTiers<NT> T, OutT* __restrict__ out, float* __re
         for (int ti = 0; ti < NT; ++ti) {
             const CombTier& t = T.t[ti];
             // 32 splits at a time: lane l holds the weight of split base+l, then the
-            // warp reads the partial rows 8 at a time, all loads in flight together
+            // warp reads the partial rows RB at a time, all loads in flight together
             for (int base = 0; base < ns[ti]; base += 32) {
                 const int k32 = base / 32;
                 float ls = -INFINITY;
@@ -786,14 +788,14 @@ decode_combine_kernel(const CombTiers<NT> T, OutT* __restrict__ out, float* __re
                 const float wl = weight(ls);
                 wl_sum += wl;
                 // the splits with weight (the rest were merged into another row or saw
-                // no key), read 8 at a time with all loads in flight together
+                // no key), read RB at a time with all loads in flight together
                 unsigned mk = __ballot_sync(0xffffffffu, wl != 0.f);
                 while (mk) {
-                    float v[8][DPL];
-                    float wt[8];
+                    float v[RB][DPL];
+                    float wt[RB];
                     const int k_first = __ffs(mk) - 1;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < RB; ++q) {
                         int k = k_first;
                         wt[q] = 0.f;
                         if (mk) {
@@ -804,7 +806,7 @@ decode_combine_kernel(const CombTiers<NT> T, OutT* __restrict__ out, float* __re
                         load_row(t.ws_o, lrow(ti, base + k), v[q]);
                     }
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) accumulate(wt[q], v[q]);
+                    for (int q = 0; q < RB; ++q) accumulate(wt[q], v[q]);
                 }
             }
             // the fix-up slots of this (sequence, head block)
@@ -941,11 +943,22 @@ attn_status launch_combine(const DecodeLaunch& L, const DecodePlan& plan, const 
     if (trace_enabled())
         trace("decode_combine_kernel<D=%d,tiers=%d,out=%s> grid=%u block=128 (one warp per (sequence, head); "
               "programmatic dependent launch)", D, NT, L.out_f32 ? "f32" : "f16", cfg.gridDim.x);
-    cudaError_t e = L.out_f32
-        ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, NT, float>, T, static_cast<float*>(L.out), L.lse, L.B,
-                             L.Hq, L.Hq / L.Hkv, plan.GH, plan.HG, plan.n_hb)
-        : cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, NT, __half>, T, static_cast<__half*>(L.out), L.lse, L.B,
-                             L.Hq, L.Hq / L.Hkv, plan.GH, plan.HG, plan.n_hb);
+    // the CUDA-core kernel's partials (no fix-up slots) come many splits to a row
+    cudaError_t e;
+    auto go = [&](auto kernel, auto* out) {
+        return cudaLaunchKernelEx(&cfg, kernel, T, out, L.lse, L.B, L.Hq, L.Hq / L.Hkv, plan.GH, plan.HG, plan.n_hb);
+    };
+    float* o32 = static_cast<float*>(L.out);
+    __half* o16 = static_cast<__half*>(L.out);
+    if constexpr (NT == 1 && D <= 128) {
+        const bool wide = T.t[0].n_fix == 0;
+        if (L.out_f32)
+            e = wide ? go(decode_combine_kernel<D, NT, float, 16>, o32) : go(decode_combine_kernel<D, NT, float, 8>, o32);
+        else
+            e = wide ? go(decode_combine_kernel<D, NT, __half, 16>, o16) : go(decode_combine_kernel<D, NT, __half, 8>, o16);
+    } else {
+        e = L.out_f32 ? go(decode_combine_kernel<D, NT, float, 8>, o32) : go(decode_combine_kernel<D, NT, __half, 8>, o16);
+    }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ATTN_ECUDA, "decode combine launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
