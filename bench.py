@@ -58,7 +58,7 @@ NCU_TRAFFIC = {
     "swa_softcap_prefill": 33.62e6,
     "paged_gqa_decode": 583.6e6,
     "int8_long_decode": 1090.79e6 + 17.94e6 + 16.94e6,   # split kernel + combine, full size
-    "chunked_prefill_paged": 190.07e6,
+    "chunked_prefill_paged": 194.92e6,
     "ring_window_decode": 542.76e6,
     "tiered_int8_decode": 652.68e6,   # cold split + hot split + combine, one call
     "paged_decode_f32io": 592.80e6,
