@@ -508,27 +508,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (W > 0) full = full && (pos - key0 < W) && (args.causal || key_last - pos < W);
             // logits in log2 units (the raw mode keeps accumulators and scales in the exponent)
             if constexpr (MODE == kModeCapped) {
-                // c*tanh(s/c): the odd Taylor polynomial through x^9 on the FMA pipe
-                // (error below 2.2e-9 for |x| <= 1/4); a warp with any element
-                // outside that range recomputes its tile with the exp/reciprocal form
+                // c*tanh(s/c) in log2 units: x times the even Taylor polynomial of
+                // tanh(x)/x through x^6, its coefficients pre-multiplied by c*log2e, on the
+                // FMA pipe (the dropped x^9 term is below 8.4e-8 for |x| <= 1/4); a warp
+                // with any element outside that range recomputes its tile with the
+                // exp/reciprocal form
                 const float2 ics = make_float2(inv_cap_scale, inv_cap_scale);
-                const float2 cl2 = make_float2(cap_log2, cap_log2);
-                bool big = false;
+                const float k1 = cap_log2 * (-1.0f / 3.0f), k2 = cap_log2 * (2.0f / 15.0f),
+                            k3 = cap_log2 * (-17.0f / 315.0f);
+                const float2 c0 = make_float2(cap_log2, cap_log2), c1 = make_float2(k1, k1),
+                             c2 = make_float2(k2, k2), c3 = make_float2(k3, k3);
+                float ax = 0.f;   // largest |x| of this thread's elements
 #pragma unroll
                 for (int i = 0; i < CW; i += 2) {
                     const float2 x = fmul2(make_float2(t[i], t[i + 1]), ics);
-                    big |= fabsf(x.x) > 0.25f || fabsf(x.y) > 0.25f;
+                    ax = fmaxf(ax, fmaxf(fabsf(x.x), fabsf(x.y)));
                     const float2 y = fmul2(x, x);
-                    float2 q = ffma2(y, make_float2(62.0f / 2835.0f, 62.0f / 2835.0f),
-                                     make_float2(-17.0f / 315.0f, -17.0f / 315.0f));
-                    q = ffma2(q, y, make_float2(2.0f / 15.0f, 2.0f / 15.0f));
-                    q = ffma2(q, y, make_float2(-1.0f / 3.0f, -1.0f / 3.0f));
-                    q = ffma2(q, y, make_float2(1.0f, 1.0f));
-                    const float2 r = fmul2(fmul2(x, q), cl2);
+                    float2 q = ffma2(y, c3, c2);
+                    q = ffma2(q, y, c1);
+                    q = ffma2(q, y, c0);
+                    const float2 r = fmul2(x, q);
                     t[i] = r.x;
                     t[i + 1] = r.y;
                 }
-                if (__any_sync(0xffffffffu, big)) {
+                if (__any_sync(0xffffffffu, !(ax <= 0.25f))) {
                     uint32_t r[CW];
 #pragma unroll
                     for (int c = 0; c < CW / 32; ++c)
