@@ -55,7 +55,7 @@ HEADLINE = "vision_2304"
 # None whenever the kernel changes after the capture.
 NCU_TRAFFIC = {
     "vision_2304": 14.24e6,
-    "swa_softcap_prefill": 33.62e6,   # softcap change re-captured: 33.615 MB read
+    "swa_softcap_prefill": 33.62e6,
     "paged_gqa_decode": 583.6e6,
     "int8_long_decode": 1090.79e6 + 17.94e6 + 16.94e6,   # split kernel + combine, full size
     "chunked_prefill_paged": 194.92e6,
