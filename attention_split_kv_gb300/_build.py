@@ -1,6 +1,6 @@
 """Build libattn.so in-tree with nvcc for sm_103a.
 
-The three CUDA translation units compile in parallel; the CUDA runtime is
+The four CUDA translation units compile in parallel; the CUDA runtime is
 linked statically so the library loads without a driver (symbol checks on a
 machine with no GPU work).
 """
@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
-SOURCES = ["api.cu", "decode.cu", "prefill.cu"]
+SOURCES = ["api.cu", "decode.cu", "decode_direct.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -113,6 +113,11 @@ struct DecodePlan {
 };
 bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys, DecodePlan* plan);
 attn_status launch_decode(const DecodeLaunch& L, const DecodePlan& plan);
+// One-launch decode (decode_direct.cu): a plain decode with the automatic split
+// plan whose sequences keep at most 512 keys, with G * D <= 1024 and a small
+// cache in all (direct_decode_fits), runs without splits or the combine.
+bool direct_decode_fits(const DecodeLaunch& L);
+attn_status launch_direct(const DecodeLaunch& L);
 attn_status launch_decode_tiered(const DecodeLaunch& cold, const DecodePlan& cold_plan, const DecodeLaunch& hot,
                                  const DecodePlan& hot_plan);
 

@@ -40,6 +40,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "decode_range.cuh"
 #include "ptx.cuh"
 
 namespace attn {
@@ -117,14 +118,6 @@ struct DecArgs {
     int* err;
 };
 
-// Range of kept keys of a sequence: [start, end).  The decode query sits at
-// position L-1, so the causal mask keeps everything below L; a window keeps
-// the W most recent tokens (run.js: kvLen = min(kvLen, W), kvStart = L - kvLen).
-__device__ __forceinline__ void seq_range(int L, int cap_eff, int W, int& start, int& end) {
-    L = min(max(L, 0), cap_eff);
-    start = (W > 0) ? max(0, L - W) : 0;
-    end = L;
-}
 enum : int { kTierPlain = 0, kTierCold = 1, kTierHot = 2 };
 
 // Kept keys [start, end) of sequence b in the index space of the call's cache
@@ -1188,6 +1181,7 @@ bool make_decode_plan(int B, int Hq, int Hkv, int D, int max_kv, int split_keys,
 }
 
 attn_status launch_decode(const DecodeLaunch& L, const DecodePlan& plan) {
+    if (direct_decode_fits(L)) return launch_direct(L);
     SplitOut so;
     attn_status st = launch_split(L, plan, &so);
     if (st != ATTN_OK) return st;

@@ -49,12 +49,15 @@ SHAPES = [
 ]
 
 
+# split_keys 0 is the automatic plan (the one-launch direct kernel for the shapes
+# whose sequences keep at most 512 keys); 16 forces the split path
+@pytest.mark.parametrize("split_keys", [0, 16], ids=["auto", "split16"])
 @pytest.mark.parametrize("int8", [False, True], ids=["f16", "int8"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%d_H%d_%d_D%d" % s[:4])
-def test_decode_contiguous(shape, int8):
+def test_decode_contiguous(shape, int8, split_keys):
     B, Hq, Hkv, D, lens = shape
     case = si.make_decode_case(B, Hq, Hkv, D, lens, seed=hash((B, Hq, D)) % 1000, int8=int8)
-    _check(case, what="contiguous %s" % (shape,))
+    _check(case, split_keys=split_keys, what="contiguous %s split %d" % (shape, split_keys))
 
 
 @pytest.mark.parametrize("page_size", [1, 8, 16, 64])
@@ -143,17 +146,19 @@ def test_split_count_does_not_change_the_result(split_keys):
 def test_decode_largest_batches(B):
     # 2048 sequences is the tensor-core kernel's limit (its prefixes live in shared
     # memory); 2049 falls back to the CUDA-core kernel; 4096 is the library's limit
+    # (an explicit split size keeps these small sequences on the split path)
     lens = [(7 * b) % 61 for b in range(B)]   # 0 .. 60 keys, some empty
     case = si.make_decode_case(B, 8, 2, 64, lens, seed=B, page_size=16)
     ref, ref_lse = oracle.decode(case)
-    got, lse = _run(case)
+    got, lse = _run(case, split_keys=16)
     assert_close(got.reshape(ref.shape), ref, what="batch %d" % B)
     assert_lse_close(lse.reshape(-1), ref_lse, what="batch %d" % B)
 
 
-def test_zero_length_sequence():
+@pytest.mark.parametrize("split_keys", [0, 16], ids=["auto", "split16"])
+def test_zero_length_sequence(split_keys):
     case = si.make_decode_case(3, 4, 2, 64, [0, 20, 0], seed=81, cap=32)
-    got, lse = _run(case)
+    got, lse = _run(case, split_keys=split_keys)
     got = got.reshape(3, 4, 64)
     assert np.all(got[0] == 0) and np.all(got[2] == 0)
     assert np.all(np.isneginf(lse[0])) and np.all(np.isneginf(lse[2]))
@@ -161,11 +166,12 @@ def test_zero_length_sequence():
     assert_close(got.reshape(ref.shape)[4:8], ref[4:8], what="zero-length neighbours")
 
 
-def test_kv_len_above_capacity_is_clamped_not_faulting():
+@pytest.mark.parametrize("split_keys", [0, 16], ids=["auto", "split16"])
+def test_kv_len_above_capacity_is_clamped_not_faulting(split_keys):
     case = si.make_decode_case(2, 4, 2, 64, [40, 64], seed=91, cap=64)
     big = case.to("cuda")
     big.kv_len = torch.tensor([40, 10_000], dtype=torch.int32, device="cuda")
-    out = attn.decode(big)
+    out = attn.decode(big, split_keys=split_keys)
     torch.cuda.synchronize()
     ref, _ = oracle.decode(case)      # same as kv_len clamped to the capacity (64)
     assert_close(out.float().cpu().numpy().reshape(ref.shape), ref, what="clamped")
@@ -190,13 +196,14 @@ def test_validate_entry_point():
     assert st == attn.ATTN_EINVAL and bad == 0
 
 
-def test_invalid_page_id_is_replaced_and_reported():
+@pytest.mark.parametrize("split_keys", [0, 16], ids=["auto", "split16"])
+def test_invalid_page_id_is_replaced_and_reported(split_keys):
     # the kernel checks every page id it uses against the pool: an id outside
     # it is replaced by page 0 (never read out of bounds) and reported
     case = si.make_decode_case(2, 4, 2, 64, [40, 30], seed=95, page_size=16).to("cuda")
     case.page_table = case.page_table.clone()
     case.page_table[0, 1] = 10_000_000
-    out = attn.decode(case)
+    out = attn.decode(case, split_keys=split_keys)
     torch.cuda.synchronize()
     assert torch.isfinite(out.float()).all()
     assert attn.attn_device_status() == attn.ATTN_EBOUNDS

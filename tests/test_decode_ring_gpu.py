@@ -50,13 +50,16 @@ RING_SHAPES = [
 ]
 
 
+# split_keys 0: the automatic plan (rings of at most 512 slots run the one-launch
+# direct kernel); 16 forces the split path, whose splits cross the ring's seam
+@pytest.mark.parametrize("split_keys", [0, 16], ids=["auto", "split16"])
 @pytest.mark.parametrize("int8", [False, True], ids=["f16", "int8"])
 @pytest.mark.parametrize("shape", RING_SHAPES, ids=lambda s: "B%d_H%d_%d_D%d_R%d_W%d" % (s[:4] + s[5:]))
-def test_ring_decode_matches_oracle(shape, int8):
+def test_ring_decode_matches_oracle(shape, int8, split_keys):
     B, Hq, Hkv, D, lens, ring, window = shape
     _, rc = _ring_case(B, Hq, Hkv, D, lens, ring, window, int8, seed=ring + D + window)
     ref, ref_lse = oracle.decode(rc)
-    got, lse = _run(rc)
+    got, lse = _run(rc, split_keys=split_keys)
     assert_close(got.reshape(ref.shape), ref, int8=int8, what="ring %s" % (shape,))
     assert_lse_close(lse.reshape(-1), ref_lse, what="ring %s" % (shape,))
 

@@ -17,8 +17,12 @@ import attention_split_kv_gb300 as attn
 import seeded_inputs as si
 attn.build(); attn.load()
 attn.prefill(si.make_prefill_case(200, 4, 2, 64, seed=1, causal=True).to("cuda"))
-attn.decode(si.make_decode_case(2, 8, 2, 128, [300, 40], seed=2, page_size=16).to("cuda"))
-attn.decode(si.make_decode_case(2, 8, 2, 128, [300, 40], seed=3, int8=True).to("cuda"))
+attn.decode(si.make_decode_case(2, 8, 2, 128, [700, 40], seed=2, page_size=16).to("cuda"))
+attn.decode(si.make_decode_case(2, 8, 2, 128, [700, 40], seed=3, int8=True).to("cuda"))
+attn.decode(si.make_decode_case(1, 4, 2, 64, [128], seed=5).to("cuda"))
+attn.decode(si.make_decode_case(1, 4, 2, 64, [128], seed=5).to("cuda"), split_keys=16)
+attn.decode(si.make_decode_case(1, 4, 2, 64, [512], seed=6).to("cuda"))
+attn.decode(si.make_decode_case(1, 4, 2, 64, [513], seed=7).to("cuda"))
 attn.prefill(si.make_prefill_case(2560, 8, 4, 256, seed=4, causal=True).to("cuda"))
 torch.cuda.synchronize()
 assert attn.attn_device_status() == attn.ATTN_OK
@@ -45,7 +49,13 @@ def test_trace_describes_every_launch():
     assert text.count("decode_combine_kernel<D=128,tiers=1,out=f16>") == 2, text
     assert "prefill_tc_kernel<D=256,mode=raw,paged=0> grid=(8,20,1)" in text, text
     assert "order=heads fastest, longest query tiles first" in text, text
-    assert len(lines) == 6, text
+    # small decodes: one launch, one CTA per (sequence, kv head), unless a split
+    # size is given or a sequence may keep more than 512 keys (capacity 520)
+    assert text.count("decode_direct_kernel<D=64,int8=0,GM=2> grid=2 block=256") == 2, text
+    assert "max_keys=128" in text and "max_keys=512" in text, text
+    assert text.count("decode_tc_kernel<D=64,NH=2,f32q=0>") == 2, text
+    assert text.count("decode_combine_kernel<D=64,tiers=1,out=f16>") == 2, text
+    assert len(lines) == 12, text
 
 
 def test_trace_is_off_by_default():
