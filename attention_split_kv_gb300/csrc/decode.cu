@@ -287,6 +287,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     auto empty_bar = [&](int s) { return smem_u32(&bars[NSLOT + s]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t kv_policy = l2_policy_evict_first();   // the cache is read once
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(full_bar(s), 1);
@@ -371,11 +372,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     row = t0 % A.ring;   // 16-token tiles never wrap: ring % 16 == 0
                 }
                 if (lane == 0) {
-                    tma_load_4d(sb + r * box_kv, &tm_k, full_bar(slot), 0, g0, row, page);
-                    tma_load_4d(sb + C::KV_BYTES + r * box_kv, &tm_v, full_bar(slot), 0, g0, row, page);
+                    tma_load_4d_hint(sb + r * box_kv, &tm_k, full_bar(slot), 0, g0, row, page, kv_policy);
+                    tma_load_4d_hint(sb + C::KV_BYTES + r * box_kv, &tm_v, full_bar(slot), 0, g0, row, page,
+                                     kv_policy);
                     if (I8) {
-                        tma_load_3d(sb + 2 * C::KV_BYTES + r * sbb, &tm_ks, full_bar(slot), row, g0, page);
-                        tma_load_3d(sb + 2 * C::KV_BYTES + C::SC_BYTES + r * sbb, &tm_vs, full_bar(slot), row, g0, page);
+                        tma_load_3d_hint(sb + 2 * C::KV_BYTES + r * sbb, &tm_ks, full_bar(slot), row, g0, page,
+                                         kv_policy);
+                        tma_load_3d_hint(sb + 2 * C::KV_BYTES + C::SC_BYTES + r * sbb, &tm_vs, full_bar(slot), row,
+                                         g0, page, kv_policy);
                     }
                 }
             }

@@ -203,6 +203,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     constexpr int NSMT = kSoftmaxWarps * 32;    // softmax threads
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t kv_policy = l2_policy_evict_first();   // the cache is read once
     if (threadIdx.x == 0) {
         for (int s = 0; s < NK; ++s) {
             mbar_init(bar(B_KFULL + s), 1);
@@ -287,8 +288,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     }
 #pragma unroll
                     for (int ch = 0; ch < NCH; ++ch)
-                        tma_load_4d(ring + slot * C::KV_BYTES + ch * C::CHUNK + bx * R * NH * 128, tm,
-                                    bar(b_full + slot), ch * 64, g0, row, page);
+                        tma_load_4d_hint(ring + slot * C::KV_BYTES + ch * C::CHUNK + bx * R * NH * 128, tm,
+                                         bar(b_full + slot), ch * 64, g0, row, page, kv_policy);
                 }
             }
             if (!ok) {
