@@ -36,11 +36,13 @@ constexpr int kDirectThreads = 256;
 constexpr int kDirectWarps = kDirectThreads / 32;
 constexpr int kDirectMaxG = kDirectMaxGD / 64;
 // Above these sizes the split path streams the cache faster than one CTA per
-// (sequence, kv head) does (measured on GB300, 8 warps a CTA): at most 2^22
-// (sequence, kv head, key, dim) elements in the call; int8 caches also at
-// most 2^15 (key, dim) elements per sequence, where the CUDA-core split
-// kernel is quicker still.
-constexpr long kDirectMaxElems = 1L << 22;
+// (sequence, kv head) does (measured on GB300): (sequence, kv head, key, dim)
+// elements in the call at most 2^24 for D = 64, 2^23 for f16 D = 128, 2^22
+// otherwise; int8 caches also at most 2^15 (key, dim) elements per sequence,
+// where the CUDA-core split kernel is quicker still.
+constexpr long direct_max_elems(int D, bool int8) {
+    return D == 64 ? (1L << 24) : (D == 128 && !int8) ? (1L << 23) : (1L << 22);
+}
 constexpr long kDirectMaxSeqElemsI8 = 1L << 15;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -376,7 +378,7 @@ bool direct_decode_fits(const DecodeLaunch& L) {
     const long n = kept_keys_bound(L);
     const long ctas = (long)L.B * L.Hkv;
     return L.split_keys == 0 && L.tier == 0 && n <= kDirectMaxKeys && (L.Hq / L.Hkv) * L.D <= kDirectMaxGD &&
-           ctas * n * L.D <= kDirectMaxElems && (!L.int8 || n * L.D <= kDirectMaxSeqElemsI8);
+           ctas * n * L.D <= direct_max_elems(L.D, L.int8) && (!L.int8 || n * L.D <= kDirectMaxSeqElemsI8);
 }
 
 attn_status launch_direct(const DecodeLaunch& L) {

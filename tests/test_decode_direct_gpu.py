@@ -2,9 +2,9 @@
 
 A plain decode with the automatic split plan (split_keys = 0) whose sequences
 keep at most 512 keys, whose query-head group times head dim is at most 1024
-and whose cache is small (at most 2^22 (sequence, kv head, key, dim) elements;
-int8: at most 2^15 (key, dim) elements per sequence) runs without splits and
-without the combine pass.  These tests compare it with the fp64 oracle over
+and whose cache is small (at most 2^22 to 2^24 (sequence, kv head, key, dim)
+elements by head dim and dtype; int8: at most 2^15 (key, dim) elements per
+sequence) runs without splits and without the combine pass.  These tests compare it with the fp64 oracle over
 every layout (contiguous, paged, ring), element type (f16 and int8 caches, f16
 and f32 queries and outputs) and option (window, softcap), at the sizes where
 the path ends, and with the split path (an explicit split_keys) on the same
@@ -155,3 +155,19 @@ def test_direct_noalloc_equals_workspace_call():
                              None, None, attn.ATTN_KV_F16, 2, 8, 2, 128, 0, 0.0, g.scale, 0, out, lse)
     torch.cuda.synchronize()
     assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["f16", "int8"])
+def test_direct_f16_valued_f32_queries_and_f32_out_are_the_f16_path(int8):
+    # q in f32 holding f16 values is the same query; f32 out holds the values the
+    # f16 path rounds
+    c16 = si.make_decode_case(3, 8, 2, 128, [200, 1, 77], seed=73, int8=int8, page_size=16)
+    c32 = si.DecodeCase(**{**c16.__dict__, "q": c16.q.float()})
+    g16, g32 = c16.to("cuda"), c32.to("cuda")
+    la = torch.empty((3, 8), dtype=torch.float32, device="cuda")
+    lb = torch.empty((3, 8), dtype=torch.float32, device="cuda")
+    a = attn.decode(g16, lse_out=la)
+    b = attn.decode(g32, lse_out=lb, out_f32=True)
+    torch.cuda.synchronize()
+    assert b.dtype == torch.float32
+    assert torch.equal(b.half(), a) and torch.equal(la, lb)
