@@ -56,12 +56,13 @@ HEADLINE = "vision_2304"
 NCU_TRAFFIC = {
     "vision_2304": 14.24e6,
     "swa_softcap_prefill": 33.62e6,
-    "paged_gqa_decode": 583.6e6,
-    "int8_long_decode": 1090.79e6 + 17.94e6 + 16.94e6,   # split kernel + combine, full size
     "chunked_prefill_paged": 194.92e6,
-    "ring_window_decode": 542.76e6,
-    "tiered_int8_decode": 652.68e6,   # cold split + hot split + combine, one call
-    "paged_decode_f32io": 592.80e6,
+    # decode: the whole call (split kernel(s) + combine), full size
+    "paged_gqa_decode": 579.24e6 + 3.34e6 + 3.12e6,
+    "int8_long_decode": 1090.74e6 + 7.55e6 + 16.94e6,
+    "ring_window_decode": 538.98e6 + 3.27e6 + 3.13e6,
+    "tiered_int8_decode": 534.05e6 + 5.32e6 + 97.76e6 + 0.26e6 + 11.63e6,   # cold split + hot split + combine
+    "paged_decode_f32io": 588.67e6 + 2.94e6 + 3.12e6,
 }
 METRIC = "decode attention KV GB/s (% of HBM peak); prefill/vision TFLOP/s (% of TC peak)"
 WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int8_long_decode",
@@ -69,6 +70,9 @@ WORKLOAD_ORDER = ["vision_2304", "paged_gqa_decode", "swa_softcap_prefill", "int
                   "tiny_decode"]
 # workloads bound by launch latency: reported as microseconds per call (lower is better)
 LATENCY_WORKLOADS = {"tiny_decode"}
+# decode workloads small enough for the library's one-launch kernel (no split, no
+# combine; the launch trace test checks that the tiny configuration takes it)
+ONE_LAUNCH_DECODE = {"tiny_decode"}
 # Nominal GB300 figures, for the second fraction of each roofline: HBM3e
 # bandwidth and the dense f16/bf16 tensor-core rate.  The fraction the targets
 # are judged on is the one against the measured peaks (`frac`).
@@ -439,7 +443,7 @@ def main(argv=None):
             out = torch.empty((c.batch, c.n_heads, c.head_dim), dtype=torch.float32 if o32 else torch.float16,
                               device=dev)
             runs[n] = (lambda c=c, ws=ws, out=out: attn.decode(c, out=out, workspace=ws))
-            work[n] = ("GB/s", decode_bytes(c, 4 if o32 else 2), "hbm", 2)
+            work[n] = ("GB/s", decode_bytes(c, 4 if o32 else 2), "hbm", 1 if n in ONE_LAUNCH_DECODE else 2)
         elif si.WORKLOADS[n]["kind"] == "tiered":
             ws = torch.empty(attn.attn_decode_tiered_workspace_size(c.batch, c.n_heads, c.n_kv_heads, c.head_dim,
                                                                     c.cap, c.hot_ring), dtype=torch.uint8,

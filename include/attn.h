@@ -104,7 +104,12 @@ size_t attn_decode_workspace_size(int batch, int n_heads, int n_kv_heads, int he
  *  softcap     c > 0 applies s -> c * tanh(s / c) after scaling; 0 = off.
  *  scale       the logit scale, e.g. 1/sqrt(D) or 1/sqrt(query_pre_attn_scalar).
  *  split_keys  keys per split (a multiple of 16), or 0 for automatic.  The
- *                result does not depend on it beyond fp32 rounding.
+ *                result does not depend on it beyond fp32 rounding.  With 0, a
+ *                call whose sequences keep at most 512 keys (max_kv, or the
+ *                window), with G * D <= 1024 and a small cache in all (at most
+ *                2^22 to 2^24 (sequence, kv head, key, dim) elements by head
+ *                dim and dtype), runs in one launch without splits or the
+ *                combine pass and leaves the workspace untouched.
  *  out         device, f16 [B, Hq, D].
  *  lse_out     device, f32 [B, Hq] or NULL: log-sum-exp of the kept scaled
  *                logits (natural log).
