@@ -42,7 +42,7 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 // accumulators; otherwise logits are scaled (and capped) first.
 enum : int { kModeRaw = 0, kModeScaled = 1, kModeCapped = 2 };
 
-constexpr int BN_OF(int D) { return (D == 64) ? 128 : 64; }
+constexpr int BN_OF(int D) { return (D == 128) ? 64 : 128; }
 
 template <int D>
 struct PrefillCfg {
@@ -63,17 +63,17 @@ struct PrefillCfg {
     static constexpr int REG_SOFTMAX = 200, REG_OTHER = 56;
     static_assert(THREADS != 256 || (REG_SOFTMAX + REG_OTHER) * 128 * CTAS_PER_SM == 65536, "register split");
     static constexpr int BN = BN_OF(D);                  // keys per tile
-    // S and P buffers in TMEM.  D=64/128 (two CTAs per SM, 256 columns each)
-    // keep one of each (D=64: S 128 + O 64 + P 64; D=128 with 64-key tiles:
-    // S 64 + O 128 + P 32): the softmax frees S as soon as its row is in
-    // registers, so the next QK^T still overlaps the exponentials.  D=256
-    // double-buffers both.
-    static constexpr int NBUF = (D <= 128) ? 1 : 2;
+    // S and P buffers in TMEM: one of each (D=64: S 128 + O 64 + P 64; D=128
+    // with 64-key tiles: S 64 + O 128 + P 32; D=256 with 128-key tiles: S 128 +
+    // O 256 + P 64 of 512): the softmax frees S as soon as its row is in
+    // registers, so the next QK^T still overlaps the exponentials.
+    static constexpr int NBUF = 1;
     // K/V ring depths: K is consumed a whole softmax earlier than V, so it gets
     // the deeper ring where shared memory allows (two D=128 CTAs per SM leave
-    // room for two of each)
-    static constexpr int KST = (D == 128) ? 2 : 3;
-    static constexpr int VST = 2;
+    // room for two of each; D=256's 64 KB Q, K and V tiles leave one of each:
+    // its QK^T then runs N = 128 MMAs, at the tensor peak, instead of N = 64)
+    static constexpr int KST = (D == 64) ? 3 : (D == 128) ? 2 : 1;
+    static constexpr int VST = (D == 256) ? 1 : 2;
     static constexpr int STAGES = KST > VST ? KST : VST;  // barrier array size
     static constexpr uint32_t Q_BYTES = NCH * BM * 128;
     static constexpr uint32_t KV_CHUNK = BN * 128;       // one 64-column box of a K or V tile
