@@ -55,7 +55,7 @@ HEADLINE = "vision_2304"
 # None whenever the kernel changes after the capture.
 NCU_TRAFFIC = {
     "vision_2304": 14.24e6,
-    "swa_softcap_prefill": 33.62e6,
+    "swa_softcap_prefill": 33.64e6,
     "chunked_prefill_paged": 194.92e6,
     # decode: the whole call (split kernel(s) + combine), full size
     "paged_gqa_decode": 579.24e6 + 3.34e6 + 3.12e6,
